@@ -1,0 +1,217 @@
+"""Pins for acceptance, prompt lookup, adaptive K, the page pool and the loop.
+
+Hand-worked fixtures under tests/golden/ cite the passage each follows;
+brute force and independent formulations cover the rest.
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import CapacityError, DenseDecoder, PagePool, accept_greedy, adapt_k, generate, ngram_propose
+from synth import workloads
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    for line in open(os.path.join(GOLD, name)):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            yield [c.strip() for c in line.split("|")]
+
+
+def _ints(s):
+    return [] if s.strip() in ("-", "") else [int(t) for t in s.split()]
+
+
+def test_accept_golden():
+    for drafts, argmax, m, committed in _rows("accept_examples.txt"):
+        got_m, got_c = accept_greedy(_ints(drafts), _ints(argmax))
+        assert got_m == int(m) and got_c == _ints(committed)
+
+
+def test_accept_brute_force_is_longest_common_prefix():
+    # Every (drafts, argmax) over a 3-letter alphabet with k <= 4.
+    for k in range(0, 5):
+        for d in itertools.product(range(3), repeat=k):
+            for a in itertools.product(range(3), repeat=k + 1):
+                m, c = accept_greedy(list(d), list(a))
+                lcp = len(os.path.commonprefix([list(d), list(a[:k])]))
+                assert m == lcp
+                assert 1 <= len(c) <= k + 1 and len(c) == m + 1
+                assert c[:m] == list(d[:m]) and c[-1] == a[m]
+
+
+def test_ngram_golden():
+    for hist, k, drafts in _rows("ngram_examples.txt"):
+        assert ngram_propose(_ints(hist), int(k), 2) == _ints(drafts), (hist, k)
+
+
+def _ngram_by_index(hist, k, n=2):
+    # Independent formulation: an incrementally built dict from each n-gram to the
+    # position of its follower, later insertions overwriting earlier ones.
+    idx = {}
+    for p in range(n, len(hist)):
+        idx[tuple(hist[p - n:p])] = p
+    if k <= 0 or len(hist) < n + 1:
+        return []
+    j = idx.get(tuple(hist[-n:]))
+    return [] if j is None else list(hist[j:min(j + k, len(hist))])
+
+
+@pytest.mark.parametrize("vocab", [3, 5, 50])
+def test_ngram_matches_hash_index_and_properties(vocab):
+    for s in range(200):
+        L = 2 + s % 60
+        hist = [int(t) for t in synth.tokens(11, f"ng{vocab}", L, vocab, offset=1000 * s)]
+        for k in (0, 1, 4, 7):
+            d = ngram_propose(hist, k)
+            assert d == _ngram_by_index(hist, k)
+            if d:
+                # the drafts follow an occurrence of the last two tokens, and no later one exists
+                starts = [j for j in range(2, L) if hist[j - 2:j] == hist[-2:] and hist[j:j + len(d)] == d]
+                assert starts and max(starts) == max(j for j in range(2, L) if hist[j - 2:j] == hist[-2:])
+                assert len(d) == min(k, L - max(starts))
+
+
+def test_adaptive_k_golden():
+    for kmax, rounds, expect in _rows("adaptive_k_trace.txt"):
+        K, got = 1, []
+        for r in rounds.split():
+            nd, m = (int(x) for x in r.split(","))
+            K = adapt_k(K, nd, m, int(kmax))
+            got.append(K)
+        assert got == _ints(expect)
+
+
+def test_adaptive_k_stays_in_range():
+    K = 1
+    for i in range(1000):
+        nd = int(synth.ints(2, "nd", 1, 0, 7, offset=i)[0])
+        m = int(synth.ints(2, "m", 1, 0, nd, offset=i)[0]) if nd else 0
+        K = adapt_k(K, nd, m, 7)
+        assert 1 <= K <= 7
+
+
+def _state(pool):
+    return [list(t) for t in pool.table], list(pool.free)
+
+
+def test_page_pool_golden():
+    pool = PagePool(7, 4, 2, 4)
+    for op, t0, t1, free in _rows("page_pool_trace.txt"):
+        name, *args = op.split()
+        args = [int(a) for a in args]
+        before = _state(pool)
+        if t0 == "error":
+            with pytest.raises((CapacityError, ValueError)):
+                getattr(pool, {"ensure": "ensure_capacity", "rewind": "rewind"}[name])(args)
+            assert _state(pool) == before
+            continue
+        if name == "ensure":
+            pool.ensure_capacity(args)
+        elif name == "advance":
+            for b, a in enumerate(args):
+                assert a <= len(pool.table[b]) * 4
+                pool.set_length(b, a)
+        else:
+            pool.rewind(args)
+        tables, fr = _state(pool)
+        assert tables[0] == _ints(t0) and tables[1] == _ints(t1) and fr == _ints(free), op
+
+
+def test_page_pool_conservation_and_undo():
+    pool = PagePool(64, 16, 4, 8)
+    for step in range(300):
+        req = [int(x) for x in synth.ints(3, "req", 4, -1, 128, offset=4 * step)]
+        pool.rewind(list(pool.length))          # tight: each table holds exactly ceil(length / 16) pages
+        before = _state(pool)
+        try:
+            pool.ensure_capacity(req)
+        except CapacityError:
+            assert _state(pool) == before
+            continue
+        if step % 3 == 0:
+            # a rewind to the lengths held before the reservation undoes it exactly
+            pool.rewind(list(pool.length))
+            assert _state(pool) == before
+            continue
+        for b, r in enumerate(req):
+            if r >= 0:
+                pool.set_length(b, r)
+        if step % 5 == 0:
+            pool.rewind([l // 2 for l in pool.length])
+        used = sorted(p for t in pool.table for p in t)
+        assert sorted(used + pool.free) == list(range(64)) and len(set(used)) == len(used)
+
+
+@pytest.fixture(scope="module")
+def tiny_model():
+    W = synth.weights(synth.TINY, 1)
+    return DenseDecoder(synth.TINY, lambda n: W[n])
+
+
+def test_spec_on_equals_spec_off(tiny_model):
+    # [PI] losslessness: spec-on equals spec-off token for token (exact in float64).
+    prompt = workloads.motif_prompt()
+    on, rec_on, _ = generate(tiny_model, [prompt], 32, drafter="ngram", k=4)
+    off, rec_off, _ = generate(tiny_model, [prompt], 32, drafter="none")
+    assert on == off and len(on[0]) == 32
+    for r in rec_on:
+        assert 1 <= len(r.committed[0]) <= len(r.spans[0])    # 1..K+1 per step
+    assert all(len(r.spans[0]) == 1 for r in rec_off)
+
+
+def test_spec_on_equals_spec_off_adaptive_table_and_batch(tiny_model):
+    prompts = [workloads.motif_prompt(), synth.tokens(8, "p2", 41, synth.TINY.vocab),
+               synth.tokens(8, "p3", 17, synth.TINY.vocab)]
+    off, _, pool_off = generate(tiny_model, prompts, 24, drafter="none", prefill_chunk=16)
+    on, rec, pool_on = generate(tiny_model, prompts, 24, drafter="ngram", adaptive=True, k_max=7,
+                                prefill_chunk=16)
+    assert on == off
+    assert all(1 <= r.k_used[b] <= 7 for r in rec for b in range(3))
+    # a table drafter that proposes the true continuation is accepted in full
+    tables = [np.array(s + [0] * 8) for s in off]          # table[j] = generated token j
+    tab, rec_t, _ = generate(tiny_model, prompts, 24, drafter="table", k=5, tables=tables, prefill_chunk=16)
+    assert tab == off
+    assert all(r.m[b] == len(r.spans[b]) - 1 for r in rec_t for b in range(3) if r.m[b] >= 0)
+
+
+def test_rewind_leaves_later_forwards_as_if_never_drafted(tiny_model):
+    # [CA] rollback == do not advance; [PI] LIFO drop of the reservation. With one
+    # sequence, the page table after each spec step equals the plain loop's table
+    # at the same length, and the cached K/V rows below the length agree.
+    prompt = workloads.motif_prompt()
+    sh = synth.TINY
+    from oracle import SeqCache
+    _, rec, pool = generate(tiny_model, [prompt], 32, drafter="table", k=4,
+                            tables=[synth.tokens(3, "junk", 64, sh.vocab)])
+    _, rec_off, pool_off = generate(tiny_model, [prompt], 32, drafter="none")
+    off_tables = {r.new_len[0]: r.page_table[0] for r in rec_off}
+    for r in rec:
+        assert r.page_table[0] == off_tables[r.new_len[0]]
+
+
+def test_truncation_at_output_budget(tiny_model):
+    # [PI] capture-shape gotcha: a span is cut to max_tokens - generated.
+    prompt = workloads.motif_prompt()
+    s, rec, _ = generate(tiny_model, [prompt], 9, drafter="table", k=7, tables=[np.arange(100)])
+    gen = 1
+    for r in rec:
+        assert len(r.spans[0]) - 1 == min(7, 9 - gen - 1)
+        gen += len(r.committed[0])
+    assert len(s[0]) == 9
+
+
+def test_oracle_reproduces_its_recorded_config1_run(tiny_model):
+    # Regression pin: the stored run was written by tests/golden/make_golden.py (oracle only).
+    rows = list(_rows("tiny_config1_oracle.txt"))
+    stream = _ints(rows[0][1])
+    s, rec, _ = generate(tiny_model, [workloads.motif_prompt(1)], 32, drafter="ngram", k=4)
+    assert s[0] == stream
+    for r, row in zip(rec, rows[1:]):
+        assert r.spans[0] == _ints(row[1]) and r.argmax[0] == _ints(row[2])
+        assert r.m[0] == int(row[3]) and r.new_len[0] == int(row[4])
