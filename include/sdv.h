@@ -1,0 +1,233 @@
+/*
+ * sdv.h -- speculative-decoding verify path on one GB300 (sm_103a).
+ *
+ * A C ABI over hand-written CUDA kernels for the draft -> verify -> accept ->
+ * commit/rewind transaction of greedy speculative decoding on a dense
+ * decoder with a paged KV cache. Plain pointers and sizes only.
+ *
+ * Sources, by page title and section:
+ *   [TS] TensorSharp, "Speculative decoding": the shared loop / trunk seam
+ *        (SpecForward, SpecEnsureCapacity, SpecRewindCache, CacheSeqLen);
+ *        the protocol (draft, verify, rollback, commit); n-gram lookup.
+ *   [PI] pegainfer, "Qwen3 DFlash speculative decoding": the transaction
+ *        (propose, verify, accept_greedy, commit/LIFO drop); draft-seed
+ *        alignment; capture-shape gotcha (span truncation, KV length read
+ *        at run time); context limit (reject cleanly).
+ *   [CA] CoreAI model zoo, "spec-decode n-gram on a dense target": dense
+ *        rollback by position; adaptive K; argmax the rows in place.
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* are device pointers; h_* are host pointers. All
+ *     device buffers are allocated by the caller and borrowed: the library
+ *     never allocates device memory and never frees what it is given. They
+ *     must stay valid for the life of the context.
+ *   - `stream` is a cudaStream_t. Every call that takes one only enqueues
+ *     work on it and returns; nothing synchronises unless stated.
+ *   - Return value: SDV_OK (0) or a negative SDV_ERR_* code. Argument errors
+ *     found on the host return at once and enqueue nothing. Errors found on
+ *     the device (a token id >= vocab, a span longer than declared, a page
+ *     table without room, a rewind past the written length, the pool out of
+ *     pages) set a device status word; kernels then skip any memory access
+ *     the error would make unsafe, and sdv_get_status reports the first
+ *     such error. No exception crosses this boundary.
+ *   - Weights are bf16, row-major W[out][in], 16-byte aligned; norm gains
+ *     are bf16 vectors. Activations are bf16 with fp32 accumulation and an
+ *     fp32 residual stream.
+ *   - A batch is B sequences, B <= max_batch; sequence b of a call is
+ *     sequence slot b of the context. Spans are packed: rows
+ *     row_off[b] .. row_off[b+1]-1 belong to sequence b (row_off[0] = 0,
+ *     row_off[B] = R, the total rows). A sequence with an empty span is left
+ *     untouched.
+ */
+#ifndef SDV_H
+#define SDV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SDV_OK 0
+#define SDV_ERR_ARG (-1)            /* invalid argument (host) or invalid span/rewind (device) */
+#define SDV_ERR_CAPACITY (-2)       /* out of pages, or past the page table / max_context */
+#define SDV_ERR_CUDA (-3)           /* a CUDA runtime call failed */
+#define SDV_ERR_DEVICE (-4)         /* bad device input: a token id outside [0, vocab), a bad page id */
+#define SDV_ERR_DEVICE_TIMEOUT (-5) /* a bounded device wait gave up */
+#define SDV_ERR_UNSUPPORTED (-6)    /* a shape this build does not handle */
+
+typedef struct sdv_ctx sdv_ctx; /* opaque; owns only host-side state */
+
+/* Decoder shape. head_dim must be 64 or 128; hidden, n_q_heads*head_dim and
+ * ffn must be multiples of 8 (16-byte rows). */
+typedef struct {
+    int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+    float rms_eps, rope_theta;
+    int qk_norm; /* 1: per-head RMSNorm on q and k before RoPE */
+} sdv_model_cfg;
+
+/* Cache and call limits. */
+typedef struct {
+    int page_size;      /* tokens per KV page (16) */
+    int n_pages;        /* pages in the pool */
+    int max_batch;      /* sequence slots */
+    int max_rows;       /* rows per sdv_spec_forward call, <= 128 */
+    int max_span;       /* rows per sequence per call, <= max_rows */
+    int max_context;    /* tokens per sequence; page table = ceil(max_context/page_size) slots */
+    int ngram_capacity; /* history tokens kept per sequence for n-gram lookup (0: none) */
+} sdv_cache_cfg;
+
+typedef struct {
+    const void *attn_norm;  /* [hidden] */
+    const void *wq;         /* [n_q_heads*head_dim][hidden] */
+    const void *wk;         /* [n_kv_heads*head_dim][hidden] */
+    const void *wv;         /* [n_kv_heads*head_dim][hidden] */
+    const void *q_norm;     /* [head_dim] */
+    const void *k_norm;     /* [head_dim] */
+    const void *wo;         /* [hidden][n_q_heads*head_dim] */
+    const void *ffn_norm;   /* [hidden] */
+    const void *w_gate;     /* [ffn][hidden] */
+    const void *w_up;       /* [ffn][hidden] */
+    const void *w_down;     /* [hidden][ffn] */
+} sdv_layer_weights;
+
+typedef struct {
+    const void *embed;              /* [vocab][hidden] */
+    const void *lm_head;            /* [vocab][hidden] (untied) */
+    const void *final_norm;         /* [hidden] */
+    const sdv_layer_weights *layers; /* host array of n_layers entries (copied at create) */
+} sdv_weights;
+
+/* Bytes of the caller-owned workspace (scratch, the device status word, page
+ * tables, lengths, the n-gram index and loop state). Allocate with 256-byte
+ * alignment; the library zero-initialises what it needs in sdv_create. */
+int sdv_workspace_bytes(const sdv_model_cfg *m, const sdv_cache_cfg *c, size_t *bytes);
+
+/* Bytes of the caller-owned KV pool. Layout (bf16):
+ *   pool[layer][page][kv (0 = K, 1 = V)][kv_head][slot (page_size)][head_dim]
+ * Token at position p of sequence b lives in page table[b][p / page_size],
+ * slot p % page_size. K is stored after head RMSNorm and RoPE. */
+int sdv_kv_pool_bytes(const sdv_model_cfg *m, const sdv_cache_cfg *c, size_t *bytes);
+
+/* Create a context on the current CUDA device. Builds TMA descriptors for the
+ * weights and activation buffers, the RoPE table, the empty page pool (every
+ * page free; the first reservation takes page 0), zero lengths and an empty
+ * n-gram index, enqueued on `stream`. The weights, pool and workspace are
+ * borrowed. Returns SDV_ERR_UNSUPPORTED on a device without sm_103a-class
+ * tcgen05 or on an unsupported shape. */
+int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights *w, void *d_kv_pool,
+               void *d_workspace, void *stream, sdv_ctx **out);
+
+/* Free the library's host state (never the borrowed device buffers). */
+int sdv_destroy(sdv_ctx *ctx);
+
+/* [TS] SpecEnsureCapacity; [PI] context limit.
+ * Reserve pages so sequence b holds d_required[b] tokens (d_required[b] < 0:
+ * leave b alone). Sequences are served in order b = 0..B-1, each filling its
+ * empty page-table slots in ascending order from the top of the free stack.
+ * All-or-nothing: if any sequence would pass its page table or the pool runs
+ * dry, nothing changes and the device status becomes SDV_ERR_CAPACITY. */
+int sdv_ensure_capacity(sdv_ctx *ctx, const int32_t *d_required, int B, void *stream);
+
+/* [PI] the transaction, Verify; [TS] SpecForward; [CA] dense rollback.
+ * One forward over each sequence's span, rows at positions L_b .. L_b+S_b-1
+ * where L_b is the cache length before the call; every row's K/V is written
+ * at its true position before any row attends, each row attends positions
+ * 0..its own, and afterwards L_b += S_b. The cache must already hold room
+ * (sdv_ensure_capacity); a span past it, S_b > max_span or R > max_rows sets
+ * the device status.
+ *   d_tokens   [R] int32 token ids; row 0 of a span is the sequence's current
+ *              token, then its drafts.
+ *   d_row_off  [B+1] int32, device-resident, so one launch shape (fixed by
+ *              max_rows / max_span) serves any mix of span lengths.
+ *   max_rows   host bound on R (<= cfg max_rows); sets the GEMM width.
+ *   max_span   host bound on every S_b (<= cfg max_span).
+ *   d_argmax   [R] int32 out: per-row argmax of the logits, lowest index on
+ *              an exact tie. Only rows < R are written.
+ *   d_logits   [R][vocab] fp32 out, or NULL. When NULL no logits are stored
+ *              anywhere: the argmax is reduced inside the LM-head kernel. */
+int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row_off, int B, int max_rows,
+                     int max_span, int32_t *d_argmax, float *d_logits, void *stream);
+
+/* [PI] the transaction, Accept; draft-seed alignment; [TS] the protocol.
+ * For each sequence with S_b = k+1 >= 1 rows (drafts d_1..d_k = span rows
+ * 1..k, argmax a_0..a_k): m_b = the largest j <= k with d_i == a_{i-1} for
+ * all i <= j. Writes d_n_accept[b] = m_b, d_committed[b*max_commit + i] =
+ * a_i for i <= m_b, d_n_commit[b] = m_b + 1, and d_new_len[b] =
+ * (L_b - S_b) + m_b + 1 with L_b the length after the forward. A sequence
+ * with an empty span gets m = -1, n_commit = 0 and new_len = -1 (pass it to
+ * sdv_rewind_cache unchanged: -1 means leave alone). The loop state of
+ * sdv_gen_init (current token, tokens generated, adaptive K) advances too.
+ * max_commit >= max_span. */
+int sdv_accept_greedy(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row_off, const int32_t *d_argmax,
+                      int B, int max_commit, int32_t *d_n_accept, int32_t *d_committed, int32_t *d_n_commit,
+                      int32_t *d_new_len, void *stream);
+
+/* [TS] SpecRewindCache; [PI] LIFO drop; [CA] rollback == do not advance.
+ * Set each length to d_length[b] (< 0: leave b alone), which must not pass
+ * the written length (else SDV_ERR_ARG in the device status, nothing
+ * changes). Rows past it stay in the pages as stale data that nothing reads.
+ * Pages past ceil(length / page_size) go back to the free stack for
+ * b = B-1 down to 0, highest slot first, so a rewind to the lengths before an
+ * sdv_ensure_capacity restores the pool exactly. */
+int sdv_rewind_cache(sdv_ctx *ctx, const int32_t *d_length, int B, void *stream);
+
+/* [TS] CacheSeqLen: copy the max_batch cache lengths into d_len. */
+int sdv_cache_seq_len(sdv_ctx *ctx, int32_t *d_len, void *stream);
+
+/* Copy the page tables (d_table[max_batch][pages_per_seq], unused slots -1),
+ * the pages held per sequence (d_n_pages[max_batch]) and the free-stack
+ * depth (d_free_top[1]) for inspection. */
+int sdv_page_table(sdv_ctx *ctx, int32_t *d_table, int32_t *d_n_pages, int32_t *d_free_top, void *stream);
+
+/* [TS] n-gram: append d_counts[b] tokens (d_tokens[b*stride + i]) to sequence
+ * b's history and insert each completed 2-gram -> follower position into
+ * that sequence's hash index (exact keys; a later insertion of the same
+ * 2-gram overwrites, so lookup returns the most recent occurrence). */
+int sdv_ngram_commit(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_counts, int B, int stride,
+                     void *stream);
+
+/* Loop state for the proposers: sequence b's current token d_first[b] (the
+ * argmax of its prompt's last row), 1 token generated, a budget of
+ * d_budget[b] generated tokens, draft length k_init, and whether K adapts.
+ * [CA] adaptive K: start at 1; +2 after a fully accepted round; -1 after any
+ * rejection; clamp to [1, k_max]; a round without drafts keeps K. */
+int sdv_gen_init(sdv_ctx *ctx, const int32_t *d_first, const int32_t *d_budget, int B, int k_init, int adaptive,
+                 int k_max, void *stream);
+
+#define SDV_DRAFT_NONE 0  /* plain one-row steps (speculation off) */
+#define SDV_DRAFT_NGRAM 1 /* 2-gram prompt lookup over the sequence's history */
+#define SDV_DRAFT_TABLE 2 /* drafts read from d_table[b*table_stride + g], g = tokens generated so far */
+
+/* Build the next verify span of every sequence from the loop state:
+ * [current, d_1..d_k] with k = min(K_b, budget_b - generated_b - 1) drafts at
+ * most ([PI] capture-shape gotcha: the span is cut to the output budget), or
+ * an empty span once the budget is met. Writes d_tokens (packed, capacity
+ * B*max_span), d_row_off [B+1] and d_required[b] = L_b + S_b (or -1) for
+ * sdv_ensure_capacity. Spans longer than max_span are cut to it. */
+int sdv_propose(sdv_ctx *ctx, int drafter, const int32_t *d_table, int table_stride, int B, int max_span,
+                int32_t *d_tokens, int32_t *d_row_off, int32_t *d_required, void *stream);
+
+/* [TS] Reset: empty sequence b's cache (all its pages return to the pool),
+ * n-gram history and loop state. */
+int sdv_reset_seq(sdv_ctx *ctx, int b, void *stream);
+
+/* Synchronise the device, copy the status word to *h_status and clear it. */
+int sdv_get_status(sdv_ctx *ctx, int32_t *h_status);
+
+/* A static string naming an SDV_* code. */
+const char *sdv_status_str(int code);
+
+/* Op-level call for parity checks at full size: paged attention of layer
+ * `layer` for the query rows d_q [R][n_q_heads][head_dim] (bf16, after RoPE)
+ * of each sequence's span, against the context's page tables and pool, with
+ * span row i of sequence b at position d_base[b] + i attending positions
+ * 0..d_base[b]+i. Writes d_out [R][n_q_heads*head_dim] bf16. */
+int sdv_op_attention(sdv_ctx *ctx, int layer, const void *d_q, const int32_t *d_row_off, const int32_t *d_base,
+                     int B, int max_span, void *d_out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SDV_H */

@@ -1,0 +1,233 @@
+"""Python binding for libsdv (include/sdv.h): the speculative-decoding verify
+path on one GB300.
+
+Argument marshalling only: every step of the path runs in the CUDA kernels
+behind the C ABI. PyTorch supplies device memory and streams. If the CUDA
+library is missing or cannot be loaded, importing the binding's entry points
+raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsdv.so")
+
+SDV_OK = 0
+SDV_ERR_ARG = -1
+SDV_ERR_CAPACITY = -2
+SDV_ERR_CUDA = -3
+SDV_ERR_DEVICE = -4
+SDV_ERR_DEVICE_TIMEOUT = -5
+SDV_ERR_UNSUPPORTED = -6
+SDV_DRAFT_NONE, SDV_DRAFT_NGRAM, SDV_DRAFT_TABLE = 0, 1, 2
+
+# Every entry point include/sdv.h declares.
+EXPORTS = (
+    "sdv_workspace_bytes", "sdv_kv_pool_bytes", "sdv_create", "sdv_destroy", "sdv_ensure_capacity",
+    "sdv_spec_forward", "sdv_accept_greedy", "sdv_rewind_cache", "sdv_cache_seq_len", "sdv_page_table",
+    "sdv_ngram_commit", "sdv_gen_init", "sdv_propose", "sdv_reset_seq", "sdv_get_status", "sdv_status_str",
+    "sdv_op_attention",
+)
+
+
+class SdvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_str(code)} ({code})")
+        self.code = code
+
+
+class ModelCfg(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("n_q_heads", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int),
+                ("vocab", ctypes.c_int), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
+                ("qk_norm", ctypes.c_int)]
+
+
+class CacheCfg(ctypes.Structure):
+    _fields_ = [("page_size", ctypes.c_int), ("n_pages", ctypes.c_int), ("max_batch", ctypes.c_int),
+                ("max_rows", ctypes.c_int), ("max_span", ctypes.c_int), ("max_context", ctypes.c_int),
+                ("ngram_capacity", ctypes.c_int)]
+
+
+LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
+
+
+class LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in LAYER_FIELDS]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("lm_head", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
+                ("layers", ctypes.POINTER(LayerWeights))]
+
+
+_lib = None
+
+
+def lib():
+    """Load libsdv.so (built by __graft_entry__.build() or build.py); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing (run the build step)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    P = ctypes.POINTER
+    L.sdv_workspace_bytes.argtypes = [P(ModelCfg), P(CacheCfg), P(sz)]
+    L.sdv_kv_pool_bytes.argtypes = [P(ModelCfg), P(CacheCfg), P(sz)]
+    L.sdv_create.argtypes = [P(ModelCfg), P(CacheCfg), P(Weights), vp, vp, vp, P(vp)]
+    L.sdv_destroy.argtypes = [vp]
+    L.sdv_ensure_capacity.argtypes = [vp, vp, i32, vp]
+    L.sdv_spec_forward.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
+    L.sdv_accept_greedy.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp]
+    L.sdv_rewind_cache.argtypes = [vp, vp, i32, vp]
+    L.sdv_cache_seq_len.argtypes = [vp, vp, vp]
+    L.sdv_page_table.argtypes = [vp, vp, vp, vp, vp]
+    L.sdv_ngram_commit.argtypes = [vp, vp, vp, i32, i32, vp]
+    L.sdv_gen_init.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp]
+    L.sdv_propose.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp, vp, vp]
+    L.sdv_reset_seq.argtypes = [vp, i32, vp]
+    L.sdv_get_status.argtypes = [vp, P(ctypes.c_int32)]
+    L.sdv_status_str.argtypes = [i32]
+    L.sdv_status_str.restype = ctypes.c_char_p
+    L.sdv_op_attention.argtypes = [vp, i32, vp, vp, vp, i32, i32, vp, vp]
+    for name in EXPORTS:
+        if name != "sdv_status_str":
+            getattr(L, name).restype = i32
+    _lib = L
+    return L
+
+
+def status_str(code: int) -> str:
+    return lib().sdv_status_str(code).decode()
+
+
+def _check(code: int, what: str):
+    if code != SDV_OK:
+        raise SdvError(code, what)
+
+
+def model_cfg(shape) -> ModelCfg:
+    return ModelCfg(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn,
+                    shape.vocab, shape.rms_eps, shape.rope_theta, 1 if shape.qk_norm else 0)
+
+
+def workspace_bytes(mcfg: ModelCfg, ccfg: CacheCfg) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().sdv_workspace_bytes(ctypes.byref(mcfg), ctypes.byref(ccfg), ctypes.byref(n)), "workspace_bytes")
+    return n.value
+
+
+def kv_pool_bytes(mcfg: ModelCfg, ccfg: CacheCfg) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().sdv_kv_pool_bytes(ctypes.byref(mcfg), ctypes.byref(ccfg), ctypes.byref(n)), "kv_pool_bytes")
+    return n.value
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def upload_bf16(bits: np.ndarray, device="cuda"):
+    """bf16 bit patterns (uint16 numpy) -> a torch bfloat16 device tensor."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+class Verifier:
+    """One context: borrowed weights, a KV pool and a workspace, all torch-owned."""
+
+    def __init__(self, shape, weights: dict, page_size=16, n_pages=1024, max_batch=1, max_rows=32, max_span=17,
+                 max_context=4096, ngram_capacity=0, stream=None):
+        import torch
+        self.shape = shape
+        self.mcfg = model_cfg(shape)
+        self.ccfg = CacheCfg(page_size, n_pages, max_batch, max_rows, max_span, max_context, ngram_capacity)
+        self.weights = weights                       # name -> torch bf16 device tensor (kept alive)
+        self.pool = torch.empty(kv_pool_bytes(self.mcfg, self.ccfg), dtype=torch.uint8, device="cuda")
+        self.workspace = torch.empty(workspace_bytes(self.mcfg, self.ccfg) + 256, dtype=torch.uint8, device="cuda")
+        base = _ptr(self.workspace)
+        self._ws_ptr = (base + 255) // 256 * 256
+        layers = (LayerWeights * shape.n_layers)()
+        for l in range(shape.n_layers):
+            for f in LAYER_FIELDS:
+                setattr(layers[l], f, _ptr(weights[f"layers.{l}.{f}"]))
+        self._layers = layers
+        self._w = Weights(_ptr(weights["embed"]), _ptr(weights["lm_head"]), _ptr(weights["final_norm"]),
+                          ctypes.cast(layers, ctypes.POINTER(LayerWeights)))
+        ctx = ctypes.c_void_p()
+        _check(lib().sdv_create(ctypes.byref(self.mcfg), ctypes.byref(self.ccfg), ctypes.byref(self._w),
+                                _ptr(self.pool), self._ws_ptr, _stream(stream), ctypes.byref(ctx)), "sdv_create")
+        self.ctx = ctx
+        self.pages_per_seq = -(-max_context // page_size)
+
+    def close(self):
+        if self.ctx:
+            lib().sdv_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # --- the ABI, one method per call (device tensors in, device tensors out)
+    def ensure_capacity(self, required, B, stream=None):
+        _check(lib().sdv_ensure_capacity(self.ctx, _ptr(required), B, _stream(stream)), "ensure_capacity")
+
+    def spec_forward(self, tokens, row_off, B, max_rows, max_span, argmax, logits=None, stream=None):
+        _check(lib().sdv_spec_forward(self.ctx, _ptr(tokens), _ptr(row_off), B, max_rows, max_span, _ptr(argmax),
+                                      _ptr(logits), _stream(stream)), "spec_forward")
+
+    def accept_greedy(self, tokens, row_off, argmax, B, max_commit, n_accept, committed, n_commit, new_len,
+                      stream=None):
+        _check(lib().sdv_accept_greedy(self.ctx, _ptr(tokens), _ptr(row_off), _ptr(argmax), B, max_commit,
+                                       _ptr(n_accept), _ptr(committed), _ptr(n_commit), _ptr(new_len),
+                                       _stream(stream)), "accept_greedy")
+
+    def rewind_cache(self, length, B, stream=None):
+        _check(lib().sdv_rewind_cache(self.ctx, _ptr(length), B, _stream(stream)), "rewind_cache")
+
+    def cache_seq_len(self, out, stream=None):
+        _check(lib().sdv_cache_seq_len(self.ctx, _ptr(out), _stream(stream)), "cache_seq_len")
+
+    def page_table(self, table, n_pages, free_top, stream=None):
+        _check(lib().sdv_page_table(self.ctx, _ptr(table), _ptr(n_pages), _ptr(free_top), _stream(stream)),
+               "page_table")
+
+    def ngram_commit(self, tokens, counts, B, stride, stream=None):
+        _check(lib().sdv_ngram_commit(self.ctx, _ptr(tokens), _ptr(counts), B, stride, _stream(stream)),
+               "ngram_commit")
+
+    def gen_init(self, first, budget, B, k_init, adaptive, k_max, stream=None):
+        _check(lib().sdv_gen_init(self.ctx, _ptr(first), _ptr(budget), B, k_init, int(adaptive), k_max,
+                                  _stream(stream)), "gen_init")
+
+    def propose(self, drafter, table, table_stride, B, max_span, tokens, row_off, required, stream=None):
+        _check(lib().sdv_propose(self.ctx, drafter, _ptr(table), table_stride, B, max_span, _ptr(tokens),
+                                 _ptr(row_off), _ptr(required), _stream(stream)), "propose")
+
+    def reset_seq(self, b, stream=None):
+        _check(lib().sdv_reset_seq(self.ctx, b, _stream(stream)), "reset_seq")
+
+    def get_status(self) -> int:
+        v = ctypes.c_int32()
+        _check(lib().sdv_get_status(self.ctx, ctypes.byref(v)), "get_status")
+        return v.value
+
+    def op_attention(self, layer, q, row_off, base, B, max_span, out, stream=None):
+        _check(lib().sdv_op_attention(self.ctx, layer, _ptr(q), _ptr(row_off), _ptr(base), B, max_span, _ptr(out),
+                                      _stream(stream)), "op_attention")
