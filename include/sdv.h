@@ -227,6 +227,17 @@ const char *sdv_status_str(int code);
 int sdv_op_attention(sdv_ctx *ctx, int layer, const void *d_q, const int32_t *d_row_off, const int32_t *d_base,
                      int B, int max_span, void *d_out, void *stream);
 
+/* Phase timing (cf. [TS] phase counters). While enabled, sdv_spec_forward
+ * records CUDA events around each launch group on its stream; this removes
+ * the launch overlap between kernels, so durations are those of each kernel
+ * run on its own. Groups: 0 prepare/embed, 1 QKV GEMM, 2 attention, 3 O GEMM,
+ * 4 gate/up GEMM, 5 down GEMM, 6 LM-head GEMM. */
+int sdv_profile_enable(sdv_ctx *ctx, int on);
+
+/* Synchronise, add the elapsed milliseconds and launch counts of every
+ * recorded group into h_ms[7] and h_count[7], and clear the record. */
+int sdv_profile_read(sdv_ctx *ctx, float *h_ms, int32_t *h_count);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,8 +30,9 @@ EXPORTS = (
     "sdv_workspace_bytes", "sdv_kv_pool_bytes", "sdv_create", "sdv_destroy", "sdv_ensure_capacity",
     "sdv_spec_forward", "sdv_accept_greedy", "sdv_rewind_cache", "sdv_cache_seq_len", "sdv_page_table",
     "sdv_ngram_commit", "sdv_gen_init", "sdv_propose", "sdv_reset_seq", "sdv_get_status", "sdv_status_str",
-    "sdv_op_attention",
+    "sdv_op_attention", "sdv_profile_enable", "sdv_profile_read",
 )
+PHASES = ("prepare", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm")
 
 
 class SdvError(RuntimeError):
@@ -96,6 +97,8 @@ def lib():
     L.sdv_status_str.argtypes = [i32]
     L.sdv_status_str.restype = ctypes.c_char_p
     L.sdv_op_attention.argtypes = [vp, i32, vp, vp, vp, i32, i32, vp, vp]
+    L.sdv_profile_enable.argtypes = [vp, i32]
+    L.sdv_profile_read.argtypes = [vp, P(ctypes.c_float), P(ctypes.c_int32)]
     for name in EXPORTS:
         if name != "sdv_status_str":
             getattr(L, name).restype = i32
@@ -227,6 +230,16 @@ class Verifier:
         v = ctypes.c_int32()
         _check(lib().sdv_get_status(self.ctx, ctypes.byref(v)), "get_status")
         return v.value
+
+    def profile_enable(self, on: bool):
+        _check(lib().sdv_profile_enable(self.ctx, int(on)), "profile_enable")
+
+    def profile_read(self):
+        """{phase: (total ms, launches)} since the last read (synchronises)."""
+        ms = (ctypes.c_float * 7)()
+        cnt = (ctypes.c_int32 * 7)()
+        _check(lib().sdv_profile_read(self.ctx, ms, cnt), "profile_read")
+        return {PHASES[i]: (ms[i], cnt[i]) for i in range(7)}
 
     def op_attention(self, layer, q, row_off, base, B, max_span, out, stream=None):
         _check(lib().sdv_op_attention(self.ctx, layer, _ptr(q), _ptr(row_off), _ptr(base), B, max_span, _ptr(out),

@@ -6,10 +6,12 @@
 // from HBM by TMA with 128-byte swizzle) and the activations are the B operand
 // (N = rows padded to 16/32/64/128, read from L2). The accumulator sits in
 // TMEM. Warp roles: warp 4 issues TMA, warp 5 issues MMAs, warps 0-3 run the
-// epilogue from tcgen05.ld. Split-K partials go to a workspace and the last
-// CTA of each tile (an atomic ticket) adds them in split order, so every
-// output element's reduction order depends only on the weight shape, never
-// on how many rows are present.
+// epilogue from tcgen05.ld. When K is split, the splits of one tile form a
+// thread-block cluster: each CTA parks its fp32 partial in its own shared
+// memory, and after a cluster barrier CTA q reduces rows q*ceil(R/splits)...
+// over distributed shared memory, adding the splits in split order. Every
+// output element's reduction order therefore depends only on the weight
+// shape, never on how many rows are present.
 #pragma once
 
 #include "common.cuh"
@@ -77,7 +79,7 @@ constexpr int kGemmThreads = 192;
 // a time (TMEM columns c0..c0+31) in v[].
 
 struct EpiSmem {
-    float rstd[128];
+    float rstd[160];
     float red[4][32];
     uint32_t am_val[4][32];
     uint32_t am_idx[4][32];
@@ -101,7 +103,7 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs &a, EpiSmem &es, float *x
     }
     const int d = f % D;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= es.rstd[c0 + j];
+    for (int j = 0; j < 32; ++j) v[j] *= es.rstd[min(c0 + j, 159)];
     if (section < 2) {
         if (a.qk_norm) {
             float sq[32];
@@ -200,7 +202,7 @@ __device__ __forceinline__ void epi_swiglu(const GemmArgs &a, EpiSmem &es, float
                                            float (&v)[32]) {
     const int f = threadIdx.x, warp = f >> 5;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= es.rstd[c0 + j];
+    for (int j = 0; j < 32; ++j) v[j] *= es.rstd[min(c0 + j, 159)];
     if (warp >= 2) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) xch[j * 64 + (f - 64)] = v[j];
@@ -228,7 +230,7 @@ __device__ __forceinline__ void epi_lmhead(const GemmArgs &a, EpiSmem &es, int t
     const int vi = tile * 128 + f;
     const bool valid = vi < a.vocab;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= es.rstd[c0 + j];
+    for (int j = 0; j < 32; ++j) v[j] *= es.rstd[min(c0 + j, 159)];
     if (a.logits != nullptr && valid) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -264,18 +266,37 @@ __device__ __forceinline__ void epi_lmhead(const GemmArgs &a, EpiSmem &es, int t
     named_bar_sync(1, 128);
 }
 
+template <int KIND>
 __device__ __forceinline__ void epi_dispatch(const GemmArgs &a, EpiSmem &es, float *xch, int tile, int c0, int R,
                                              float (&v)[32]) {
-    switch (a.kind) {
-        case EPI_QKV: epi_qkv(a, es, xch, tile, c0, R, v); break;
-        case EPI_RESID: epi_resid(a, es, tile, c0, R, v); break;
-        case EPI_SWIGLU: epi_swiglu(a, es, xch, tile, c0, R, v); break;
-        default: epi_lmhead(a, es, tile, c0, R, v); break;
-    }
+    if constexpr (KIND == EPI_QKV) epi_qkv(a, es, xch, tile, c0, R, v);
+    else if constexpr (KIND == EPI_RESID) epi_resid(a, es, tile, c0, R, v);
+    else if constexpr (KIND == EPI_SWIGLU) epi_swiglu(a, es, xch, tile, c0, R, v);
+    else epi_lmhead(a, es, tile, c0, R, v);
 }
 
 // ------------------------------------------------------------------ kernel
-template <int N>
+template <int KIND>
+__device__ __forceinline__ void load_a(uint8_t *sa, const CUtensorMap *tmA0, const CUtensorMap *tmA1,
+                                       const CUtensorMap *tmA2, uint64_t *bar, const GemmArgs &a, int tile, int kc,
+                                       uint64_t pol) {
+    if constexpr (KIND == EPI_SWIGLU) {
+        // rows 0-63: gate features tile*64.., rows 64-127: the same up features
+        tma_load_2d_hint(sa, tmA0, bar, kc, tile * 64, pol);
+        tma_load_2d_hint(sa + 8192, tmA1, bar, kc, tile * 64, pol);
+    } else if constexpr (KIND == EPI_QKV) {
+        if (tile < a.q_tiles)
+            tma_load_2d_hint(sa, tmA0, bar, kc, tile * 128, pol);
+        else if (tile < a.q_tiles + a.k_tiles)
+            tma_load_2d_hint(sa, tmA1, bar, kc, (tile - a.q_tiles) * 128, pol);
+        else
+            tma_load_2d_hint(sa, tmA2, bar, kc, (tile - a.q_tiles - a.k_tiles) * 128, pol);
+    } else {
+        tma_load_2d_hint(sa, tmA0, bar, kc, tile * 128, pol);
+    }
+}
+
+template <int N, int KIND>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
@@ -291,6 +312,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int kb0 = split * a.kps;
     const int kb1 = min(kb0 + a.kps, a.k_blocks);
     const int nk = kb1 - kb0;
+    const bool clustered = a.splits > 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S::STAGES; ++s) {
@@ -317,6 +339,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // Let the next kernel in the stream start its prologue now.
     pdl_trigger();
 
+    // partial tile for the cluster reduction: [N rows][128 features] fp32 at the start
+    // of the stage memory; exchange buffers for the epilogues after it.
+    float *red = reinterpret_cast<float *>(smem);
+    float *xch = reinterpret_cast<float *>(smem + N * 512);
+
     if (warp == 4) {
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
@@ -324,21 +351,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int pre = min(nk, S::STAGES);
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(&full_bar[i], S::STAGE_BYTES);
-                uint8_t *sa = smem + i * S::STAGE_BYTES;
-                const int kc = (kb0 + i) * 64;
-                if (a.kind == EPI_SWIGLU) {
-                    tma_load_2d_hint(sa, &tmA0, &full_bar[i], kc, tile * 64, pol_w);
-                    tma_load_2d_hint(sa + 8192, &tmA1, &full_bar[i], kc, tile * 64, pol_w);
-                } else if (a.kind == EPI_QKV) {
-                    if (tile < a.q_tiles)
-                        tma_load_2d_hint(sa, &tmA0, &full_bar[i], kc, tile * 128, pol_w);
-                    else if (tile < a.q_tiles + a.k_tiles)
-                        tma_load_2d_hint(sa, &tmA1, &full_bar[i], kc, (tile - a.q_tiles) * 128, pol_w);
-                    else
-                        tma_load_2d_hint(sa, &tmA2, &full_bar[i], kc, (tile - a.q_tiles - a.k_tiles) * 128, pol_w);
-                } else {
-                    tma_load_2d_hint(sa, &tmA0, &full_bar[i], kc, tile * 128, pol_w);
-                }
+                load_a<KIND>(smem + i * S::STAGE_BYTES, &tmA0, &tmA1, &tmA2, &full_bar[i], a, tile, (kb0 + i) * 64,
+                             pol_w);
             }
             pdl_wait();  // activations come from the previous kernel
             for (int i = 0; i < pre; ++i)
@@ -353,19 +367,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 mbar_arrive_expect_tx(&full_bar[s], S::STAGE_BYTES);
                 uint8_t *sa = smem + s * S::STAGE_BYTES;
                 const int kc = (kb0 + i) * 64;
-                if (a.kind == EPI_SWIGLU) {
-                    tma_load_2d_hint(sa, &tmA0, &full_bar[s], kc, tile * 64, pol_w);
-                    tma_load_2d_hint(sa + 8192, &tmA1, &full_bar[s], kc, tile * 64, pol_w);
-                } else if (a.kind == EPI_QKV) {
-                    if (tile < a.q_tiles)
-                        tma_load_2d_hint(sa, &tmA0, &full_bar[s], kc, tile * 128, pol_w);
-                    else if (tile < a.q_tiles + a.k_tiles)
-                        tma_load_2d_hint(sa, &tmA1, &full_bar[s], kc, (tile - a.q_tiles) * 128, pol_w);
-                    else
-                        tma_load_2d_hint(sa, &tmA2, &full_bar[s], kc, (tile - a.q_tiles - a.k_tiles) * 128, pol_w);
-                } else {
-                    tma_load_2d_hint(sa, &tmA0, &full_bar[s], kc, tile * 128, pol_w);
-                }
+                load_a<KIND>(sa, &tmA0, &tmA1, &tmA2, &full_bar[s], a, tile, kc, pol_w);
                 tma_load_2d(sa + S::A_BYTES, &tmB, &full_bar[s], kc, 0);
             }
         }
@@ -388,15 +390,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             umma_commit(&accum_bar);
         }
-    } else {
-        // ---------------- epilogue warps 0-3
+    }
+
+    int R = 0;
+    if (warp < 4) {
+        // ---------------- epilogue warps 0-3: rstd rows, then the accumulator
         pdl_wait();
-        int R = *a.nrows;
+        R = *a.nrows;
         if (R > N) {
             set_status(a.status, SDV_ERR_ARG);
             R = N;
         }
-        if (a.kind != EPI_RESID) {
+        if constexpr (KIND != EPI_RESID) {
             const int r = threadIdx.x;
             if (r < N) {
                 float s = 0.f;
@@ -411,48 +416,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!mbar_wait(&accum_bar, 0)) set_status(a.status, SDV_ERR_DEVICE_TIMEOUT);
         tc_fence_after();
         const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        float *xch = reinterpret_cast<float *>(smem);  // stage buffers are free once the accumulator is final
         float v[32];
-        if (a.splits > 1) {
+        if (clustered) {
             const int f = threadIdx.x;
             for (int c0 = 0; c0 < R; c0 += 32) {
                 tmem_ld32(taddr + c0, v);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int r = c0 + j;
-                    if (r < R)
-                        a.partial[(static_cast<size_t>(split) * a.rows_cap + r) * a.part_stride + tile * 128 + f] =
-                            v[j];
-                }
-            }
-            __threadfence();
-            named_bar_sync(1, 128);
-            if (threadIdx.x == 0) es.last = (atomicAdd(&a.counters[tile], 1) == a.splits - 1) ? 1 : 0;
-            named_bar_sync(1, 128);
-            if (es.last) {
-                __threadfence();
-                for (int c0 = 0; c0 < R; c0 += 32) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int r = c0 + j;
-                        float s = 0.f;
-                        if (r < R)
-                            for (int sp = 0; sp < a.splits; ++sp)
-                                s += __ldcg(&a.partial[(static_cast<size_t>(sp) * a.rows_cap + r) * a.part_stride +
-                                                       tile * 128 + f]);
-                        v[j] = s;
-                    }
-                    epi_dispatch(a, es, xch, tile, c0, R, v);
-                }
-                if (threadIdx.x == 0) a.counters[tile] = 0;
+                for (int j = 0; j < 32; ++j)
+                    if (c0 + j < R) red[(c0 + j) * 128 + f] = v[j];
             }
         } else {
             for (int c0 = 0; c0 < R; c0 += 32) {
                 tmem_ld32(taddr + c0, v);
-                epi_dispatch(a, es, xch, tile, c0, R, v);
+                epi_dispatch<KIND>(a, es, xch, tile, c0, R, v);
             }
         }
-        if (a.kind == EPI_LMHEAD) {
+    }
+    if (clustered) {
+        // every partial of the tile is parked in its CTA's shared memory
+        cluster_sync();
+        if (warp < 4) {
+            const int f = threadIdx.x;
+            const int per = (R + a.splits - 1) / a.splits;
+            const int s0 = min(R, static_cast<int>(cluster_ctarank()) * per), s1 = min(R, s0 + per);
+            const uint32_t red_local = smem_u32(red);
+            float v[32];
+            for (int c0 = s0; c0 < s1; c0 += 32) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                for (int q = 0; q < a.splits; ++q) {  // fixed split order
+                    const uint32_t base = mapa_shared(red_local, static_cast<uint32_t>(q));
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (c0 + j < s1) v[j] += ld_dsmem(base + static_cast<uint32_t>(((c0 + j) * 128 + f) * 4));
+                }
+                epi_dispatch<KIND>(a, es, xch, tile, c0, s1, v);
+            }
+        }
+        // no CTA leaves while its partial may still be read
+        cluster_sync();
+    }
+    if constexpr (KIND == EPI_LMHEAD) {
+        if (warp < 4) {
             __threadfence();
             named_bar_sync(1, 128);
             if (threadIdx.x == 0)

@@ -3,6 +3,7 @@
 // spec_forward, accept, ensure_capacity, rewind, n-gram and propose.
 #include <cmath>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -47,9 +48,10 @@ GemmPlan make_plan(int tiles, int k_blocks, int sm_count) {
     GemmPlan p;
     p.tiles = tiles;
     p.k_blocks = k_blocks;
-    // Split K so that tiles x splits covers the SMs; depends only on the weight shape.
+    // Split K so that tiles x splits covers the SMs; depends only on the weight shape. The
+    // splits of a tile run as one thread-block cluster, so at most 8 (the portable size).
     int splits = ceil_div(sm_count, tiles);
-    splits = std::max(1, std::min(splits, std::max(1, k_blocks / 2)));
+    splits = std::max(1, std::min({splits, std::max(1, k_blocks / 2), 8}));
     p.kps = ceil_div(k_blocks, splits);
     p.splits = ceil_div(k_blocks, p.kps);
     return p;
@@ -84,7 +86,50 @@ struct sdv_ctx {
     CUtensorMap tm_xb[4]{}, tm_ao[4]{}, tm_h[4]{};
     bool use_pdl = true;
     int gen_adaptive = 0, gen_kmax = 1;  // adaptive-K settings from sdv_gen_init
+    // phase timing
+    bool profiling = false;
+    std::vector<cudaEvent_t> ev_pool;
+    std::vector<std::pair<int, std::pair<int, int>>> ev_marks;  // (group, (start event, stop event))
+    size_t ev_used = 0;
+    ~sdv_ctx() {
+        for (cudaEvent_t e : ev_pool) cudaEventDestroy(e);
+    }
 };
+
+namespace {
+cudaEvent_t next_event(sdv_ctx *ctx) {
+    if (ctx->ev_used == ctx->ev_pool.size()) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        ctx->ev_pool.push_back(e);
+    }
+    return ctx->ev_pool[ctx->ev_used++];
+}
+// Marks one launch group when profiling; no-op otherwise.
+struct PhaseMark {
+    sdv_ctx *ctx;
+    int group, i0 = -1;
+    cudaStream_t st;
+    PhaseMark(sdv_ctx *c, int g, cudaStream_t s) : ctx(c), group(g), st(s) {
+        if (ctx->profiling) {
+            cudaEvent_t e = next_event(ctx);
+            if (e) {
+                i0 = static_cast<int>(ctx->ev_used - 1);
+                cudaEventRecord(e, st);
+            }
+        }
+    }
+    ~PhaseMark() {
+        if (ctx->profiling && i0 >= 0) {
+            cudaEvent_t e = next_event(ctx);
+            if (e) {
+                cudaEventRecord(e, st);
+                ctx->ev_marks.push_back({group, {i0, static_cast<int>(ctx->ev_used - 1)}});
+            }
+        }
+    }
+};
+}  // namespace
 
 namespace {
 
@@ -255,14 +300,69 @@ cudaError_t launch(const sdv_ctx *ctx, void (*kern)(KArgs...), dim3 grid, dim3 b
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+template <int N, int KIND>
+cudaError_t launch_gemm_nk(const sdv_ctx *ctx, const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &a2,
+                           const CUtensorMap &b, const GemmArgs &args, int grid, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = GemmShape<N>::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (ctx->use_pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (args.splits > 1) {  // the K splits of a tile form one cluster
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = args.splits;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<N, KIND>, a0, a1, a2, b, args);
+}
+
+template <int KIND>
+cudaError_t launch_gemm_k(const sdv_ctx *ctx, int nidx, const CUtensorMap &a0, const CUtensorMap &a1,
+                          const CUtensorMap &a2, const CUtensorMap &b, const GemmArgs &args, int grid,
+                          cudaStream_t st) {
+    switch (nidx) {
+        case 0: return launch_gemm_nk<16, KIND>(ctx, a0, a1, a2, b, args, grid, st);
+        case 1: return launch_gemm_nk<32, KIND>(ctx, a0, a1, a2, b, args, grid, st);
+        case 2: return launch_gemm_nk<64, KIND>(ctx, a0, a1, a2, b, args, grid, st);
+        default: return launch_gemm_nk<128, KIND>(ctx, a0, a1, a2, b, args, grid, st);
+    }
+}
+
 cudaError_t launch_gemm(const sdv_ctx *ctx, int nidx, const CUtensorMap &a0, const CUtensorMap &a1,
                         const CUtensorMap &a2, const CUtensorMap &b, const GemmArgs &args, int grid, cudaStream_t st) {
-    switch (nidx) {
-        case 0: return launch(ctx, gemm_kernel<16>, dim3(grid), dim3(kGemmThreads), GemmShape<16>::SMEM_BYTES, st, a0, a1, a2, b, args);
-        case 1: return launch(ctx, gemm_kernel<32>, dim3(grid), dim3(kGemmThreads), GemmShape<32>::SMEM_BYTES, st, a0, a1, a2, b, args);
-        case 2: return launch(ctx, gemm_kernel<64>, dim3(grid), dim3(kGemmThreads), GemmShape<64>::SMEM_BYTES, st, a0, a1, a2, b, args);
-        default: return launch(ctx, gemm_kernel<128>, dim3(grid), dim3(kGemmThreads), GemmShape<128>::SMEM_BYTES, st, a0, a1, a2, b, args);
+    switch (args.kind) {
+        case EPI_QKV: return launch_gemm_k<EPI_QKV>(ctx, nidx, a0, a1, a2, b, args, grid, st);
+        case EPI_RESID: return launch_gemm_k<EPI_RESID>(ctx, nidx, a0, a1, a2, b, args, grid, st);
+        case EPI_SWIGLU: return launch_gemm_k<EPI_SWIGLU>(ctx, nidx, a0, a1, a2, b, args, grid, st);
+        default: return launch_gemm_k<EPI_LMHEAD>(ctx, nidx, a0, a1, a2, b, args, grid, st);
     }
+}
+
+template <int N>
+cudaError_t set_gemm_smem() {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<N, EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         GemmShape<N>::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_kernel<N, EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GemmShape<N>::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_kernel<N, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GemmShape<N>::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(gemm_kernel<N, EPI_LMHEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GemmShape<N>::SMEM_BYTES);
+    return e;
 }
 
 int rc(cudaError_t e) { return e == cudaSuccess ? SDV_OK : SDV_ERR_CUDA; }
@@ -400,7 +500,7 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, gemm_kernel<16>) != cudaSuccess) {
+    if (cudaFuncGetAttributes(&fa, gemm_kernel<16, EPI_QKV>) != cudaSuccess) {
         cudaGetLastError();
         return SDV_ERR_UNSUPPORTED;  // no sm_103a image for this device
     }
@@ -452,10 +552,10 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
     }
 
     cudaError_t e = cudaSuccess;
-    e = cudaFuncSetAttribute(gemm_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmShape<16>::SMEM_BYTES);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmShape<32>::SMEM_BYTES);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmShape<64>::SMEM_BYTES);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmShape<128>::SMEM_BYTES);
+    e = set_gemm_smem<16>();
+    if (e == cudaSuccess) e = set_gemm_smem<32>();
+    if (e == cudaSuccess) e = set_gemm_smem<64>();
+    if (e == cudaSuccess) e = set_gemm_smem<128>();
     if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_partial_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnShape<128>::SMEM);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_partial_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnShape<64>::SMEM);
     if (e != cudaSuccess) {
@@ -510,7 +610,11 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const sdv_model_cfg &m = ctx->m;
     const int ni = n_index(max_rows);
-    int r = prepare(ctx, d_tokens, d_row_off, nullptr, B, max_rows, max_span, 1, st);
+    int r;
+    {
+        PhaseMark pm(ctx, 0, st);
+        r = prepare(ctx, d_tokens, d_row_off, nullptr, B, max_rows, max_span, 1, st);
+    }
     if (r) return r;
     for (int l = 0; l < m.n_layers; ++l) {
         const sdv_layer_weights &L = ctx->layers[l];
@@ -535,10 +639,17 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
         a.n_pages = ctx->c.n_pages;
         a.q_out = ctx->q;
         a.kv_layer = ctx->pool + ctx->layer_stride * l;
-        if (launch_gemm(ctx, ni, ctx->tm_wq[l], ctx->tm_wk[l], ctx->tm_wv[l], ctx->tm_xb[ni], a,
-                        ctx->plan[P_QKV].tiles * ctx->plan[P_QKV].splits, st) != cudaSuccess)
-            return SDV_ERR_CUDA;
-        r = run_attention(ctx, l, ctx->q, ctx->attn_o, max_rows, max_span, st);
+        cudaError_t e;
+        {
+            PhaseMark pm(ctx, 1, st);
+            e = launch_gemm(ctx, ni, ctx->tm_wq[l], ctx->tm_wk[l], ctx->tm_wv[l], ctx->tm_xb[ni], a,
+                            ctx->plan[P_QKV].tiles * ctx->plan[P_QKV].splits, st);
+        }
+        if (e != cudaSuccess) return SDV_ERR_CUDA;
+        {
+            PhaseMark pm(ctx, 2, st);
+            r = run_attention(ctx, l, ctx->q, ctx->attn_o, max_rows, max_span, st);
+        }
         if (r) return r;
         // O projection + residual; emits bf16(x * g_ffn) and sum-of-squares parts
         a = base_args(ctx, EPI_RESID, P_O);
@@ -547,16 +658,22 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
         a.xb = ctx->xb;
         a.g_next = static_cast<const bf16 *>(L.ffn_norm);
         a.ss_out = ctx->ss;
-        if (launch_gemm(ctx, ni, ctx->tm_wo[l], ctx->tm_wo[l], ctx->tm_wo[l], ctx->tm_ao[ni], a,
-                        ctx->plan[P_O].tiles * ctx->plan[P_O].splits, st) != cudaSuccess)
-            return SDV_ERR_CUDA;
+        {
+            PhaseMark pm(ctx, 3, st);
+            e = launch_gemm(ctx, ni, ctx->tm_wo[l], ctx->tm_wo[l], ctx->tm_wo[l], ctx->tm_ao[ni], a,
+                            ctx->plan[P_O].tiles * ctx->plan[P_O].splits, st);
+        }
+        if (e != cudaSuccess) return SDV_ERR_CUDA;
         // gate/up projection + SwiGLU
         a = base_args(ctx, EPI_SWIGLU, P_GU);
         a.n_out = m.ffn;
         a.h_out = ctx->h;
-        if (launch_gemm(ctx, ni, ctx->tm_wg[l], ctx->tm_wu[l], ctx->tm_wg[l], ctx->tm_xb[ni], a,
-                        ctx->plan[P_GU].tiles * ctx->plan[P_GU].splits, st) != cudaSuccess)
-            return SDV_ERR_CUDA;
+        {
+            PhaseMark pm(ctx, 4, st);
+            e = launch_gemm(ctx, ni, ctx->tm_wg[l], ctx->tm_wu[l], ctx->tm_wg[l], ctx->tm_xb[ni], a,
+                            ctx->plan[P_GU].tiles * ctx->plan[P_GU].splits, st);
+        }
+        if (e != cudaSuccess) return SDV_ERR_CUDA;
         // down projection + residual; emits bf16(x * g_next) for the next layer (or the final norm)
         a = base_args(ctx, EPI_RESID, P_DOWN);
         a.n_out = m.hidden;
@@ -564,9 +681,12 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
         a.xb = ctx->xb;
         a.g_next = static_cast<const bf16 *>(l + 1 < m.n_layers ? ctx->layers[l + 1].attn_norm : ctx->w.final_norm);
         a.ss_out = ctx->ss;
-        if (launch_gemm(ctx, ni, ctx->tm_wd[l], ctx->tm_wd[l], ctx->tm_wd[l], ctx->tm_h[ni], a,
-                        ctx->plan[P_DOWN].tiles * ctx->plan[P_DOWN].splits, st) != cudaSuccess)
-            return SDV_ERR_CUDA;
+        {
+            PhaseMark pm(ctx, 5, st);
+            e = launch_gemm(ctx, ni, ctx->tm_wd[l], ctx->tm_wd[l], ctx->tm_wd[l], ctx->tm_h[ni], a,
+                            ctx->plan[P_DOWN].tiles * ctx->plan[P_DOWN].splits, st);
+        }
+        if (e != cudaSuccess) return SDV_ERR_CUDA;
     }
     // final norm (folded as a per-row scale) + LM head + per-row argmax
     GemmArgs a = base_args(ctx, EPI_LMHEAD, P_LM);
@@ -575,10 +695,13 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
     a.argmax_out = d_argmax;
     a.done_counter = ctx->done_lm;
     a.vocab = m.vocab;
-    if (launch_gemm(ctx, ni, ctx->tm_lm, ctx->tm_lm, ctx->tm_lm, ctx->tm_xb[ni], a,
-                    ctx->plan[P_LM].tiles * ctx->plan[P_LM].splits, st) != cudaSuccess)
-        return SDV_ERR_CUDA;
-    return SDV_OK;
+    cudaError_t e;
+    {
+        PhaseMark pm(ctx, 6, st);
+        e = launch_gemm(ctx, ni, ctx->tm_lm, ctx->tm_lm, ctx->tm_lm, ctx->tm_xb[ni], a,
+                        ctx->plan[P_LM].tiles * ctx->plan[P_LM].splits, st);
+    }
+    return e == cudaSuccess ? SDV_OK : SDV_ERR_CUDA;
 }
 
 int sdv_accept_greedy(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row_off, const int32_t *d_argmax,
@@ -687,6 +810,29 @@ const char *sdv_status_str(int code) {
         case SDV_ERR_UNSUPPORTED: return "unsupported";
         default: return "unknown status";
     }
+}
+
+int sdv_profile_enable(sdv_ctx *ctx, int on) {
+    if (!ctx) return SDV_ERR_ARG;
+    ctx->profiling = on != 0;
+    return SDV_OK;
+}
+
+int sdv_profile_read(sdv_ctx *ctx, float *h_ms, int32_t *h_count) {
+    if (!ctx || !h_ms || !h_count) return SDV_ERR_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return SDV_ERR_CUDA;
+    for (const auto &mk : ctx->ev_marks) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, ctx->ev_pool[mk.second.first], ctx->ev_pool[mk.second.second]) != cudaSuccess)
+            return SDV_ERR_CUDA;
+        if (mk.first >= 0 && mk.first < 7) {
+            h_ms[mk.first] += ms;
+            h_count[mk.first] += 1;
+        }
+    }
+    ctx->ev_marks.clear();
+    ctx->ev_used = 0;
+    return SDV_OK;
 }
 
 int sdv_op_attention(sdv_ctx *ctx, int layer, const void *d_q, const int32_t *d_row_off, const int32_t *d_base,
