@@ -1,13 +1,17 @@
 // Paged grouped-query attention for the verify span.
 //
-// Each sequence's keys 0 .. L_b+S_b-1 are cut into fixed chunks of positions
-// (the cut depends on positions only, never on the span length). One CTA takes
-// one (sequence, chunk, kv head): it stages the query rows of the kv head's
-// q-head group (grp heads x span rows, one 16-row MMA tile per warp) and
-// streams the chunk's K/V pages in 64-key blocks, running an online softmax
-// with the causal limit "row i attends positions <= L_b + i". The KV length
-// is read from device memory at run time. A second kernel merges the chunk
-// partials (m, l, o) in chunk order with a log-sum-exp rescale.
+// Keys are cut by position only (never by span length): 128-key chunks, and
+// groups of 8 chunks (1024 positions). A group of one sequence and one kv
+// head is one work item, run by a thread-block cluster of 8 CTAs: CTA c loads
+// chunk c of the group (its K/V pages, one shot) and the query rows of the kv
+// head's q-head group (grp heads x span rows, one 16-row MMA tile per warp),
+// and runs the softmax with the causal limit "row i attends positions <=
+// L_b + i" (L_b is read from device memory at run time). The 8 chunk partials
+// (m, l, o) are merged over distributed shared memory in chunk order. A
+// sequence of one group writes its output there; longer sequences park one
+// partial per group in global memory, and for each row slice the last group
+// to arrive merges all groups in group order. Every row's reduction order is
+// thus fixed by positions alone.
 #pragma once
 
 #include "common.cuh"
@@ -21,30 +25,32 @@ struct AttnArgs {
     int pages_per_seq, page_size, n_pages;
     const int *seq_base;     // [B] cache length before the span
     const int *row_off;      // [B+1]
-    const int *work;         // [n] (b << 16) | chunk
-    const int *work_off;     // [B+1] first work item of each sequence
+    const int *work;         // [n] (b << 16) | group
     const int *n_work;       // [1]
-    const int *row_seq;      // [rows] sequence of each packed row
-    const int *nrows;        // [1]
     int nq, nkv, D, grp;
-    int chunk;               // keys per work item (multiple of 64)
     int q0, qrows;           // span rows q0 .. q0+qrows-1 handled by this launch
     float scale_log2;        // log2(e) / sqrt(D)
-    float *part_o;           // [work][nkv][grp*qrows][D]
-    float2 *part_ml;         // [work][nkv][grp*qrows]
+    float *part_o;           // [work][nkv][grp*qrows][D]  group partials (unnormalised o)
+    float2 *part_ml;         // [work][nkv][grp*qrows]     (m, l)
+    int *counters;           // [max_batch][nkv][kAttnCluster] group arrivals per row slice
     bf16 *out;               // [rows][nq*D]
     int *status;
 };
 
-constexpr int kAttnThreads = 256;  // 8 warps, one 16-row query tile each
-constexpr int kAttnKB = 64;        // keys per streamed block
+constexpr int kAttnThreads = 256;   // 8 warps, one 16-row query tile each
+constexpr int kAttnKB = 64;         // keys per MMA block
+constexpr int kAttnChunk = 128;     // keys per CTA
+constexpr int kAttnCluster = 8;     // CTAs (chunks) per work item
+constexpr int kAttnGroup = kAttnChunk * kAttnCluster;
 
 template <int D>
 struct AttnShape {
     static constexpr int ROW_BYTES = D * 2;
     static constexpr int Q_BYTES = 128 * ROW_BYTES;
-    static constexpr int KV_BYTES = kAttnKB * ROW_BYTES;            // one of K or V, one block
-    static constexpr int SMEM = Q_BYTES + 4 * KV_BYTES + 128;       // Q + double-buffered K and V
+    static constexpr int KV_BYTES = kAttnChunk * ROW_BYTES;       // K (or V) of one chunk
+    static constexpr int SMEM = Q_BYTES + 2 * KV_BYTES + 128 * 8;  // Q, K, V, (m, l) of 128 rows
+    // after the softmax the K/V region holds the fp32 partial o [128 rows][D]
+    static_assert(2 * KV_BYTES >= 128 * D * 4, "partial must fit in the K/V region");
 };
 
 // byte offset of 16-byte chunk `c` of row `r` in a row-major tile with an XOR swizzle
@@ -58,10 +64,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool v
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int n>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
-}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -84,54 +87,73 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&p);
 }
+__device__ __forceinline__ float ld_dsmem_rank(const void *local, uint32_t rank) {
+    return ld_dsmem(mapa_shared(smem_u32(local), rank));
+}
 
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 2) attn_partial_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs a) {
     using S = AttnShape<D>;
     constexpr int CH = D / 8;  // 16-byte chunks per row
     extern __shared__ __align__(128) uint8_t sm[];
     uint8_t *sQ = sm;
-    const uint32_t sK0 = smem_u32(sm + S::Q_BYTES);                 // K buffers 0/1, then V buffers 0/1
-    const uint32_t sV0 = smem_u32(sm + S::Q_BYTES + 2 * S::KV_BYTES);
+    const uint32_t sK = smem_u32(sm + S::Q_BYTES);
+    const uint32_t sV = smem_u32(sm + S::Q_BYTES + S::KV_BYTES);
+    float *po_s = reinterpret_cast<float *>(sm + S::Q_BYTES);                 // after compute: [128][D]
+    float2 *ml_s = reinterpret_cast<float2 *>(sm + S::Q_BYTES + 2 * S::KV_BYTES);
+    __shared__ int last_s;
+    __shared__ int page_s[kAttnChunk];  // page ids of the chunk's positions (at most one per key)
 
     pdl_trigger();
     pdl_wait();
-    const int w = blockIdx.x, g = blockIdx.y;
+    const int w = blockIdx.x / kAttnCluster, g = blockIdx.y;
+    const int cr = static_cast<int>(cluster_ctarank());
+    // Both early exits depend only on (w, b), which the 8 CTAs of a cluster share,
+    // so a cluster leaves whole and never waits on a departed CTA.
     if (w >= *a.n_work) return;
-    const int b = a.work[w] >> 16, c = a.work[w] & 0xffff;
+    const int b = a.work[w] >> 16, grp_idx = a.work[w] & 0xffff;
     const int L = a.seq_base[b];
     const int S_b = a.row_off[b + 1] - a.row_off[b];
-    const int ni = min(S_b - a.q0, a.qrows);
-    if (ni <= 0) return;
+    const int ni = max(0, min(S_b - a.q0, a.qrows));
+    if (ni == 0) return;
     const int M = a.grp * ni;
     const int key_end = L + S_b;
-    const int k0 = c * a.chunk;
-    const int k1 = min(k0 + a.chunk, key_end);
-    const int nblk = (k1 - k0 + kAttnKB - 1) / kAttnKB;
+    const int n_groups = (key_end + kAttnGroup - 1) / kAttnGroup;
+    const int k0 = (grp_idx * kAttnCluster + cr) * kAttnChunk;
+    const int k1 = min(k0 + kAttnChunk, key_end);
+    const int nblk = k1 > k0 ? (k1 - k0 + kAttnKB - 1) / kAttnKB : 0;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t head_stride = static_cast<size_t>(a.page_size) * D;
+    const int Mpad = (M + 15) & ~15;
 
-    // stage Q rows j = i_local * grp + hh (row i = q0 + i_local of the span, head g*grp + hh)
-    for (int e = tid; e < 128 * CH; e += kAttnThreads) {
-        const int j = e / CH, ch = e % CH;
-        const bool valid = j < M;
-        const bf16 *src = a.q;
-        if (valid) {
-            const int r = a.row_off[b] + a.q0 + j / a.grp;
-            const int h = g * a.grp + j % a.grp;
-            src = a.q + (static_cast<size_t>(r) * a.nq + h) * D + ch * 8;
+    // stage Q rows j = i_local * grp + hh (span row q0 + i_local, head g*grp + hh), and the chunk's K/V
+    if (nblk > 0) {
+        for (int e = tid; e < Mpad * CH; e += kAttnThreads) {
+            const int j = e / CH, ch = e % CH;
+            const bool valid = j < M;
+            const bf16 *src = a.q;
+            if (valid) {
+                const int r = a.row_off[b] + a.q0 + j / a.grp;
+                const int h = g * a.grp + j % a.grp;
+                src = a.q + (static_cast<size_t>(r) * a.nq + h) * D + ch * 8;
+            }
+            cp_async16(smem_u32(sQ) + swz<D>(j, ch), src, valid);
         }
-        cp_async16(smem_u32(sQ) + swz<D>(j, ch), src, valid);
-    }
-    auto load_kv = [&](int blk, int buf) {
-        for (int e = tid; e < kAttnKB * CH; e += kAttnThreads) {
+        const int nkeys = nblk * kAttnKB;
+        // page id of every page the chunk touches, looked up once
+        const int pg0 = k0 / a.page_size, npg = (k1 - 1) / a.page_size - pg0 + 1;
+        for (int i = tid; i < npg; i += kAttnThreads) {
+            const int slot_idx = pg0 + i;
+            page_s[i] = slot_idx < a.pages_per_seq ? a.page_table[b * a.pages_per_seq + slot_idx] : -1;
+        }
+        __syncthreads();
+        for (int e = tid; e < nkeys * CH; e += kAttnThreads) {
             const int key = e / CH, ch = e % CH;
-            const int u = k0 + blk * kAttnKB + key;
+            const int u = k0 + key;
             bool valid = u < k1;
             const bf16 *srcK = a.kv_layer, *srcV = a.kv_layer;
             if (valid) {
-                const int slot_idx = u / a.page_size;
-                const int page = slot_idx < a.pages_per_seq ? a.page_table[b * a.pages_per_seq + slot_idx] : -1;
+                const int page = page_s[u / a.page_size - pg0];
                 if (page < 0 || page >= a.n_pages) {
                     set_status(a.status, SDV_ERR_CAPACITY);
                     valid = false;
@@ -142,17 +164,17 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_partial_kernel(const Att
                     srcV = a.kv_layer + base + static_cast<size_t>(a.nkv) * head_stride;
                 }
             }
-            cp_async16(sK0 + buf * S::KV_BYTES + swz<D>(key, ch), srcK, valid);
-            cp_async16(sV0 + buf * S::KV_BYTES + swz<D>(key, ch), srcV, valid);
+            cp_async16(sK + swz<D>(key, ch), srcK, valid);
+            cp_async16(sV + swz<D>(key, ch), srcV, valid);
         }
         cp_async_commit();
-    };
-    load_kv(0, 0);  // commit group 0 holds Q and the first K/V block
+        cp_async_wait_all();
+    }
+    __syncthreads();
 
     const int mt = warp;                  // 16-row query tile of this warp
-    const bool active = mt * 16 < M;
+    const bool active = nblk > 0 && mt * 16 < M;
     const int gq = lane >> 2, tq = lane & 3;
-    // causal limits of this thread's two rows (gq and gq + 8 of the tile)
     const int jr0 = mt * 16 + gq, jr1 = jr0 + 8;
     const int lim0 = L + a.q0 + jr0 / a.grp, lim1 = L + a.q0 + jr1 / a.grp;
 
@@ -161,17 +183,8 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_partial_kernel(const Att
     for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    for (int blk = 0; blk < nblk; ++blk) {
-        const int buf = blk & 1;
-        if (blk + 1 < nblk) {
-            load_kv(blk + 1, buf ^ 1);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        if (active) {
-            // scores for 64 keys: 8 n-tiles of 8 keys
+    if (active) {
+        for (int blk = 0; blk < nblk; ++blk) {
             float s[8][4];
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
@@ -186,10 +199,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_partial_kernel(const Att
 #pragma unroll
                 for (int nt = 0; nt < 8; nt += 2) {
                     const int i = lane >> 3;
-                    const int key = nt * 8 + (i >> 1) * 8 + (lane & 7);
+                    const int key = blk * kAttnKB + nt * 8 + (i >> 1) * 8 + (lane & 7);
                     const int ch = ks * 2 + (i & 1);
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(sK0 + buf * S::KV_BYTES + swz<D>(key, ch), b0, b1, b2, b3);
+                    ldsm_x4(sK + swz<D>(key, ch), b0, b1, b2, b3);
                     mma_bf16_16816(s[nt], qa, b0, b1);
                     mma_bf16_16816(s[nt + 1], qa, b2, b3);
                 }
@@ -243,10 +256,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_partial_kernel(const Att
 #pragma unroll
                 for (int dn = 0; dn < D / 8; dn += 2) {
                     const int i = lane >> 3;
-                    const int key = kk * 16 + (i & 1) * 8 + (lane & 7);
+                    const int key = blk * kAttnKB + kk * 16 + (i & 1) * 8 + (lane & 7);
                     const int ch = dn + (i >> 1);
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(sV0 + buf * S::KV_BYTES + swz<D>(key, ch), b0, b1, b2, b3);
+                    ldsm_x4_t(sV + swz<D>(key, ch), b0, b1, b2, b3);
                     mma_bf16_16816(o[dn], pa, b0, b1);
                     mma_bf16_16816(o[dn + 1], pa, b2, b3);
                 }
@@ -258,55 +271,88 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_partial_kernel(const Att
             l0 = l0 * al0 + rs0;
             l1 = l1 * al1 + rs1;
         }
-        __syncthreads();  // the buffer is refilled next iteration
     }
+    __syncthreads();  // K/V no longer read: the region now holds this chunk's partial
 
-    if (active) {
-        const size_t rowsw = static_cast<size_t>(a.grp) * a.qrows;
-        const size_t slot = static_cast<size_t>(w) * a.nkv + g;  // one partial per (work item, kv head)
-        float *po = a.part_o + slot * rowsw * D;
-        float2 *pml = a.part_ml + slot * rowsw;
-        if (jr0 < M) {
+    // chunk partial -> own shared memory ([row][D] fp32 and (m, l)); rows without keys stay (-inf, 0, 0)
+    if (mt * 16 < Mpad) {
 #pragma unroll
-            for (int dn = 0; dn < D / 8; ++dn)
-                *reinterpret_cast<float2 *>(&po[static_cast<size_t>(jr0) * D + dn * 8 + tq * 2]) =
-                    make_float2(o[dn][0], o[dn][1]);
-            if (tq == 0) pml[jr0] = make_float2(m0, l0);
+        for (int dn = 0; dn < D / 8; ++dn) {
+            *reinterpret_cast<float2 *>(&po_s[jr0 * D + dn * 8 + tq * 2]) = make_float2(o[dn][0], o[dn][1]);
+            *reinterpret_cast<float2 *>(&po_s[jr1 * D + dn * 8 + tq * 2]) = make_float2(o[dn][2], o[dn][3]);
         }
-        if (jr1 < M) {
-#pragma unroll
-            for (int dn = 0; dn < D / 8; ++dn)
-                *reinterpret_cast<float2 *>(&po[static_cast<size_t>(jr1) * D + dn * 8 + tq * 2]) =
-                    make_float2(o[dn][2], o[dn][3]);
-            if (tq == 0) pml[jr1] = make_float2(m1, l1);
+        if (tq == 0) {
+            ml_s[jr0] = make_float2(m0, l0);
+            ml_s[jr1] = make_float2(m1, l1);
         }
     }
-}
+    cluster_sync();
 
-// One CTA per (packed row, kv head); thread d of the block handles dim d of each head in the group.
-__global__ void attn_combine_kernel(const AttnArgs a) {
-    pdl_trigger();
-    pdl_wait();
-    const int r = blockIdx.x, g = blockIdx.y, d = threadIdx.x;
-    if (r >= *a.nrows) return;
-    const int b = a.row_seq[r];
-    const int i = r - a.row_off[b];
-    if (i < a.q0 || i >= a.q0 + a.qrows) return;
-    const int w0 = a.work_off[b], w1 = a.work_off[b + 1];
+    // merge the 8 chunks of the group for this CTA's row slice, chunk order 0..7
+    const int per = (M + kAttnCluster - 1) / kAttnCluster;
+    const int r0 = min(M, cr * per), r1 = min(M, r0 + per);
     const size_t rowsw = static_cast<size_t>(a.grp) * a.qrows;
-    for (int hh = 0; hh < a.grp; ++hh) {
-        const int j = (i - a.q0) * a.grp + hh;
-        float M = -INFINITY;
-        for (int w = w0; w < w1; ++w) M = fmaxf(M, a.part_ml[(w * a.nkv + g) * rowsw + j].x);
-        float num = 0.f, den = 0.f;
-        for (int w = w0; w < w1; ++w) {
-            const size_t slot = (static_cast<size_t>(w) * a.nkv + g) * rowsw + j;
-            const float2 ml = a.part_ml[slot];
-            const float sc = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-            den += sc * ml.y;
-            num += sc * a.part_o[slot * a.D + d];
+    const size_t slot = static_cast<size_t>(w) * a.nkv + g;
+    for (int e = tid; e < (r1 - r0) * D; e += kAttnThreads) {
+        const int j = r0 + e / D, d = e % D;
+        float mq[kAttnCluster];
+        float Mx = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < kAttnCluster; ++q) {
+            mq[q] = ld_dsmem_rank(&ml_s[j].x, static_cast<uint32_t>(q));
+            Mx = fmaxf(Mx, mq[q]);
         }
-        a.out[static_cast<size_t>(r) * a.nq * a.D + (g * a.grp + hh) * a.D + d] = __float2bfloat16(num / den);
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int q = 0; q < kAttnCluster; ++q) {
+            const float sc = mq[q] == -INFINITY ? 0.f : exp2f(mq[q] - Mx);
+            den += sc * ld_dsmem_rank(&ml_s[j].y, static_cast<uint32_t>(q));
+            num += sc * ld_dsmem_rank(&po_s[j * D + d], static_cast<uint32_t>(q));
+        }
+        const int r = a.row_off[b] + a.q0 + j / a.grp;
+        const int h = g * a.grp + j % a.grp;
+        if (n_groups == 1) {
+            a.out[(static_cast<size_t>(r) * a.nq + h) * D + d] = __float2bfloat16(num / den);
+        } else {
+            a.part_o[(slot * rowsw + j) * D + d] = num;
+            if (d == 0) a.part_ml[slot * rowsw + j] = make_float2(Mx, den);
+        }
+    }
+    cluster_sync();  // no CTA leaves while its partial may still be read
+
+    if (n_groups > 1) {
+        // the last group to finish this row slice merges every group, in group order
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            int *cnt = &a.counters[(b * a.nkv + g) * kAttnCluster + cr];
+            last_s = atomicAdd(cnt, 1) == n_groups - 1;
+            if (last_s) *cnt = 0;
+        }
+        __syncthreads();
+        if (last_s) {
+            __threadfence();
+            const int wfirst = w - grp_idx;  // the work items of one sequence are consecutive
+            for (int e = tid; e < (r1 - r0) * D; e += kAttnThreads) {
+                const int j = r0 + e / D, d = e % D;
+                float Mx = -INFINITY;
+                for (int gi = 0; gi < n_groups; ++gi) {
+                    const size_t sl = (static_cast<size_t>(wfirst + gi) * a.nkv + g) * rowsw + j;
+                    Mx = fmaxf(Mx, __ldcg(&a.part_ml[sl].x));
+                }
+                float num = 0.f, den = 0.f;
+                for (int gi = 0; gi < n_groups; ++gi) {
+                    const size_t sl = (static_cast<size_t>(wfirst + gi) * a.nkv + g) * rowsw + j;
+                    const float2 ml = __ldcg(&a.part_ml[sl]);
+                    const float sc = ml.x == -INFINITY ? 0.f : exp2f(ml.x - Mx);
+                    den += sc * ml.y;
+                    num += sc * __ldcg(&a.part_o[sl * D + d]);
+                }
+                const int r = a.row_off[b] + a.q0 + j / a.grp;
+                const int h = g * a.grp + j % a.grp;
+                a.out[(static_cast<size_t>(r) * a.nq + h) * D + d] = __float2bfloat16(num / den);
+            }
+        }
     }
 }
 

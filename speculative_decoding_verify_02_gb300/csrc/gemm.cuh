@@ -63,7 +63,7 @@ struct GemmShape {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = N * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES_RAW = (110 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES_RAW = (104 * 1024) / STAGE_BYTES;  // two CTAs per SM
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
     static constexpr int TMEM_COLS = N < 32 ? 32 : N;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
@@ -75,204 +75,147 @@ struct GemmShape {
 constexpr int kGemmThreads = 192;
 
 // ------------------------------------------------------------------ epilogues
-// Each epilogue thread owns one output feature (TMEM lane) and sees 32 rows at
-// a time (TMEM columns c0..c0+31) in v[].
+// One warp finishes one row at a time. Lane l holds features l, l+32, l+64 and
+// l+96 of the 128-feature tile in x[0..3]: every rotate-half pair of a head and
+// every gate/up pair of the SwiGLU tile then sits inside one lane, and the row
+// reductions (head norm, sum of squares, argmax) are warp reductions. The code
+// is small on purpose: each SM runs one CTA of a launch, with a cold
+// instruction cache.
 
 struct EpiSmem {
-    float rstd[160];
-    float red[4][32];
-    uint32_t am_val[4][32];
-    uint32_t am_idx[4][32];
+    float rstd[128];
     int last;
 };
 
-__device__ __forceinline__ void epi_qkv(const GemmArgs &a, EpiSmem &es, float *xch, int tile, int c0, int R,
-                                        float (&v)[32]) {
-    const int f = threadIdx.x, warp = f >> 5, lane = f & 31;
-    const int D = a.D, half = D >> 1;
-    int section, head;  // 0 = q, 1 = k, 2 = v
+__device__ __forceinline__ void epi_qkv_row(const GemmArgs &a, float rstd, int tile, int r, int lane, float (&x)[4]) {
+    const int D = a.D;
+    int section, fbase;  // 0 = q, 1 = k, 2 = v; first feature of the tile inside its section
     if (tile < a.q_tiles) {
         section = 0;
-        head = (tile * 128 + f) / D;
+        fbase = tile * 128;
     } else if (tile < a.q_tiles + a.k_tiles) {
         section = 1;
-        head = ((tile - a.q_tiles) * 128 + f) / D;
+        fbase = (tile - a.q_tiles) * 128;
     } else {
         section = 2;
-        head = ((tile - a.q_tiles - a.k_tiles) * 128 + f) / D;
+        fbase = (tile - a.q_tiles - a.k_tiles) * 128;
     }
-    const int d = f % D;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= es.rstd[min(c0 + j, 159)];
+    for (int i = 0; i < 4; ++i) x[i] *= rstd;
+    const int pos = a.row_pos[r];
     if (section < 2) {
-        if (a.qk_norm) {
-            float sq[32];
+        const bf16 *gain = section == 0 ? a.q_gain : a.k_gain;
+        const int p = pos < 0 ? 0 : (pos >= a.rope_rows ? a.rope_rows - 1 : pos);
+        if (D == 128) {  // one head: dims l, l+32, l+64, l+96; pairs (l, l+64), (l+32, l+96)
+            if (a.qk_norm) {
+                const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
+                const float sc = rsqrtf(ss / 128.f + a.eps);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) sq[j] = v[j] * v[j];
-            es.red[warp][lane] = transpose_sum32(sq, lane);
-            named_bar_sync(1, 128);
-            const int wph = D >> 5;               // warps per head
-            const int w0 = (warp / wph) * wph;
-            const float g = __bfloat162float(section == 0 ? a.q_gain[d] : a.k_gain[d]);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                float s = 0.f;
-                for (int w = w0; w < w0 + wph; ++w) s += es.red[w][j];
-                v[j] *= rsqrtf(s / static_cast<float>(D) + a.eps) * g;
+                for (int i = 0; i < 4; ++i) x[i] *= sc * __bfloat162float(gain[lane + 32 * i]);
             }
-            named_bar_sync(1, 128);
-        }
-        // rotate-half RoPE: pair (d, d + D/2)
-#pragma unroll
-        for (int j = 0; j < 32; ++j) xch[j * 128 + f] = v[j];
-        named_bar_sync(1, 128);
-        const int partner = d < half ? f + half : f - half;
-        const int jj = d < half ? d : d - half;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int r = c0 + j;
-            if (r < R) {
-                int pos = a.row_pos[r];
-                pos = pos < 0 ? 0 : (pos >= a.rope_rows ? a.rope_rows - 1 : pos);
-                const float2 cs = a.rope[static_cast<size_t>(pos) * half + jj];
-                const float u = xch[j * 128 + partner];
-                v[j] = d < half ? v[j] * cs.x - u * cs.y : v[j] * cs.x + u * cs.y;
+            const float2 c0 = a.rope[static_cast<size_t>(p) * 64 + lane];
+            const float2 c1 = a.rope[static_cast<size_t>(p) * 64 + lane + 32];
+            const float y0 = x[0] * c0.x - x[2] * c0.y, y2 = x[2] * c0.x + x[0] * c0.y;
+            const float y1 = x[1] * c1.x - x[3] * c1.y, y3 = x[3] * c1.x + x[1] * c1.y;
+            x[0] = y0; x[1] = y1; x[2] = y2; x[3] = y3;
+        } else {  // D == 64, two heads: (x0, x1) dims l, l+32 of one head, (x2, x3) of the next
+            if (a.qk_norm) {
+                const float sa = rsqrtf(warp_sum(x[0] * x[0] + x[1] * x[1]) / 64.f + a.eps);
+                const float sb = rsqrtf(warp_sum(x[2] * x[2] + x[3] * x[3]) / 64.f + a.eps);
+                const float g0 = __bfloat162float(gain[lane]), g1 = __bfloat162float(gain[lane + 32]);
+                x[0] *= sa * g0; x[1] *= sa * g1; x[2] *= sb * g0; x[3] *= sb * g1;
             }
+            const float2 c = a.rope[static_cast<size_t>(p) * 32 + lane];
+            const float y0 = x[0] * c.x - x[1] * c.y, y1 = x[1] * c.x + x[0] * c.y;
+            const float y2 = x[2] * c.x - x[3] * c.y, y3 = x[3] * c.x + x[2] * c.y;
+            x[0] = y0; x[1] = y1; x[2] = y2; x[3] = y3;
         }
-        named_bar_sync(1, 128);
     }
     if (section == 0) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int r = c0 + j;
-            if (r < R) a.q_out[(static_cast<size_t>(r) * a.nq + head) * D + d] = __float2bfloat16(v[j]);
+        for (int i = 0; i < 4; ++i) {
+            const int fs = fbase + lane + 32 * i;
+            a.q_out[(static_cast<size_t>(r) * a.nq + fs / D) * D + fs % D] = __float2bfloat16(x[i]);
         }
-    } else {
-        const int kvsel = section - 1;
+        return;
+    }
+    const int seq = a.row_seq[r], slot_idx = pos / a.page_size;
+    int page = -1;
+    if (seq >= 0 && pos >= 0 && slot_idx < a.pages_per_seq)
+        page = a.page_table[static_cast<size_t>(seq) * a.pages_per_seq + slot_idx];
+    if (page < 0 || page >= a.n_pages) {
+        if (lane == 0) set_status(a.status, SDV_ERR_CAPACITY);
+        return;
+    }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int r = c0 + j;
-            if (r < R) {
-                const int seq = a.row_seq[r], pos = a.row_pos[r];
-                const int slot_idx = pos / a.page_size;
-                int page = -1;
-                if (seq >= 0 && pos >= 0 && slot_idx < a.pages_per_seq)
-                    page = a.page_table[static_cast<size_t>(seq) * a.pages_per_seq + slot_idx];
-                if (page < 0 || page >= a.n_pages) {
-                    set_status(a.status, SDV_ERR_CAPACITY);
-                } else {
-                    const size_t off =
-                        ((((static_cast<size_t>(page) * 2 + kvsel) * a.nkv + head) * a.page_size + pos % a.page_size) *
-                         D) +
-                        d;
-                    a.kv_layer[off] = __float2bfloat16(v[j]);
-                }
-            }
-        }
+    for (int i = 0; i < 4; ++i) {
+        const int fs = fbase + lane + 32 * i;
+        const size_t off =
+            (((static_cast<size_t>(page) * 2 + (section - 1)) * a.nkv + fs / D) * a.page_size + pos % a.page_size) * D +
+            fs % D;
+        a.kv_layer[off] = __float2bfloat16(x[i]);
     }
 }
 
-__device__ __forceinline__ void epi_resid(const GemmArgs &a, EpiSmem &es, int tile, int c0, int R, float (&v)[32]) {
-    const int f = threadIdx.x, warp = f >> 5, lane = f & 31;
-    const int F = tile * 128 + f;
-    const bool valid = F < a.n_out;
-    const float g = valid ? __bfloat162float(a.g_next[F]) : 0.f;
-    float sq[32];
+__device__ __forceinline__ void epi_resid_row(const GemmArgs &a, int tile, int r, int lane, float (&x)[4]) {
+    float sq = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const int r = c0 + j;
-        sq[j] = 0.f;
-        if (valid && r < R) {
-            const size_t o = static_cast<size_t>(r) * a.hidden + F;
-            const float xn = a.x[o] + v[j];
-            a.x[o] = xn;
-            a.xb[o] = __float2bfloat16(xn * g);
-            sq[j] = xn * xn;
-        }
-    }
-    es.red[warp][lane] = transpose_sum32(sq, lane);
-    named_bar_sync(1, 128);
-    if (f < 32 && c0 + f < R)
-        a.ss_out[static_cast<size_t>(tile) * a.rows_cap + c0 + f] =
-            (es.red[0][f] + es.red[1][f]) + (es.red[2][f] + es.red[3][f]);
-    named_bar_sync(1, 128);
-}
-
-__device__ __forceinline__ void epi_swiglu(const GemmArgs &a, EpiSmem &es, float *xch, int tile, int c0, int R,
-                                           float (&v)[32]) {
-    const int f = threadIdx.x, warp = f >> 5;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= es.rstd[min(c0 + j, 159)];
-    if (warp >= 2) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) xch[j * 64 + (f - 64)] = v[j];
-    }
-    named_bar_sync(1, 128);
-    if (warp < 2) {
-        const int F = tile * 64 + f;
+    for (int i = 0; i < 4; ++i) {
+        const int F = tile * 128 + lane + 32 * i;
         if (F < a.n_out) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int r = c0 + j;
-                if (r < R) {
-                    const float gt = v[j], up = xch[j * 64 + f];
-                    const float act = gt / (1.f + __expf(-gt));
-                    a.h_out[static_cast<size_t>(r) * a.n_out + F] = __float2bfloat16(act * up);
-                }
-            }
+            const size_t o = static_cast<size_t>(r) * a.hidden + F;
+            const float xn = a.x[o] + x[i];
+            a.x[o] = xn;
+            a.xb[o] = __float2bfloat16(xn * __bfloat162float(a.g_next[F]));
+            sq += xn * xn;
         }
     }
-    named_bar_sync(1, 128);
+    sq = warp_sum(sq);
+    if (lane == 0) a.ss_out[static_cast<size_t>(tile) * a.rows_cap + r] = sq;
 }
 
-__device__ __forceinline__ void epi_lmhead(const GemmArgs &a, EpiSmem &es, int tile, int c0, int R, float (&v)[32]) {
-    const int f = threadIdx.x, warp = f >> 5, lane = f & 31;
-    const int vi = tile * 128 + f;
-    const bool valid = vi < a.vocab;
+__device__ __forceinline__ void epi_swiglu_row(const GemmArgs &a, float rstd, int tile, int r, int lane,
+                                               float (&x)[4]) {
+    // gate features tile*64 + (l, l+32) in x0, x1; the matching up features in x2, x3
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] *= es.rstd[min(c0 + j, 159)];
-    if (a.logits != nullptr && valid) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-            if (c0 + j < R) a.logits[static_cast<size_t>(c0 + j) * a.vocab + vi] = v[j];
-    }
-    uint32_t my_val = 0, my_idx = 0xffffffffu;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const uint32_t u = valid ? orderable(v[j]) : 0u;
-        const uint32_t m = __reduce_max_sync(0xffffffffu, u);
-        const uint32_t cand = (valid && u == m) ? static_cast<uint32_t>(vi) : 0xffffffffu;
-        const uint32_t idx = __reduce_min_sync(0xffffffffu, cand);
-        if (lane == j) {
-            my_val = m;
-            my_idx = idx;
+    for (int i = 0; i < 2; ++i) {
+        const int F = tile * 64 + lane + 32 * i;
+        if (F < a.n_out) {
+            const float gt = x[i] * rstd, up = x[i + 2] * rstd;
+            a.h_out[static_cast<size_t>(r) * a.n_out + F] = __float2bfloat16(gt / (1.f + __expf(-gt)) * up);
         }
     }
-    es.am_val[warp][lane] = my_val;
-    es.am_idx[warp][lane] = my_idx;
-    named_bar_sync(1, 128);
-    if (f < 32 && c0 + f < R) {
-        uint32_t bv = es.am_val[0][f], bi = es.am_idx[0][f];
+}
+
+__device__ __forceinline__ void epi_lmhead_row(const GemmArgs &a, float rstd, int tile, int r, int lane,
+                                               float (&x)[4]) {
+    uint32_t best = 0, bidx = 0xffffffffu;
 #pragma unroll
-        for (int w = 1; w < 4; ++w) {
-            const uint32_t cv = es.am_val[w][f], ci = es.am_idx[w][f];
-            if (cv > bv || (cv == bv && ci < bi)) {
-                bv = cv;
-                bi = ci;
+    for (int i = 0; i < 4; ++i) {  // ascending vocabulary index: the first maximum is the lowest index
+        const int v = tile * 128 + lane + 32 * i;
+        if (v < a.vocab) {
+            const float y = x[i] * rstd;
+            if (a.logits != nullptr) a.logits[static_cast<size_t>(r) * a.vocab + v] = y;
+            const uint32_t u = orderable(y);
+            if (bidx == 0xffffffffu || u > best) {
+                best = u;
+                bidx = static_cast<uint32_t>(v);
             }
         }
-        atomicMax(&a.keys[c0 + f], (static_cast<unsigned long long>(bv) << 32) | (0xffffffffull - bi));
     }
-    named_bar_sync(1, 128);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, best);
+    const uint32_t idx = __reduce_min_sync(0xffffffffu, best == m ? bidx : 0xffffffffu);
+    if (lane == 0 && idx != 0xffffffffu)
+        atomicMax(&a.keys[r], (static_cast<unsigned long long>(m) << 32) | (0xffffffffull - idx));
 }
 
 template <int KIND>
-__device__ __forceinline__ void epi_dispatch(const GemmArgs &a, EpiSmem &es, float *xch, int tile, int c0, int R,
-                                             float (&v)[32]) {
-    if constexpr (KIND == EPI_QKV) epi_qkv(a, es, xch, tile, c0, R, v);
-    else if constexpr (KIND == EPI_RESID) epi_resid(a, es, tile, c0, R, v);
-    else if constexpr (KIND == EPI_SWIGLU) epi_swiglu(a, es, xch, tile, c0, R, v);
-    else epi_lmhead(a, es, tile, c0, R, v);
+__device__ __forceinline__ void epi_row(const GemmArgs &a, const EpiSmem &es, int tile, int r, int lane,
+                                        float (&x)[4]) {
+    if constexpr (KIND == EPI_QKV) epi_qkv_row(a, es.rstd[r], tile, r, lane, x);
+    else if constexpr (KIND == EPI_RESID) epi_resid_row(a, tile, r, lane, x);
+    else if constexpr (KIND == EPI_SWIGLU) epi_swiglu_row(a, es.rstd[r], tile, r, lane, x);
+    else epi_lmhead_row(a, es.rstd[r], tile, r, lane, x);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -296,8 +239,30 @@ __device__ __forceinline__ void load_a(uint8_t *sa, const CUtensorMap *tmA0, con
     }
 }
 
+template <int KIND>
+__device__ __forceinline__ void prefetch_a(const CUtensorMap *tmA0, const CUtensorMap *tmA1, const CUtensorMap *tmA2,
+                                           const GemmArgs &a, int tile, int kc) {
+    if constexpr (KIND == EPI_SWIGLU) {
+        tma_prefetch_2d(tmA0, kc, tile * 64);
+        tma_prefetch_2d(tmA1, kc, tile * 64);
+    } else if constexpr (KIND == EPI_QKV) {
+        if (tile < a.q_tiles)
+            tma_prefetch_2d(tmA0, kc, tile * 128);
+        else if (tile < a.q_tiles + a.k_tiles)
+            tma_prefetch_2d(tmA1, kc, (tile - a.q_tiles) * 128);
+        else
+            tma_prefetch_2d(tmA2, kc, (tile - a.q_tiles - a.k_tiles) * 128);
+    } else {
+        tma_prefetch_2d(tmA0, kc, tile * 128);
+    }
+}
+
+// k-blocks of weights each CTA pulls into L2 ahead of its pipeline before waiting on the
+// previous kernel (none for the LM head, whose 778 MB would only thrash L2)
+constexpr int kL2AheadBlocks = 16;
+
 template <int N, int KIND>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads, 2)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
     using S = GemmShape<N>;
@@ -339,10 +304,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // Let the next kernel in the stream start its prologue now.
     pdl_trigger();
 
-    // partial tile for the cluster reduction: [N rows][128 features] fp32 at the start
-    // of the stage memory; exchange buffers for the epilogues after it.
+    // the accumulator tile as [N rows][128 features] fp32, in the stage memory (free once the
+    // accumulator is final); in a cluster the other CTAs read it over DSMEM.
     float *red = reinterpret_cast<float *>(smem);
-    float *xch = reinterpret_cast<float *>(smem + N * 512);
 
     if (warp == 4) {
         if (lane == 0) {
@@ -353,6 +317,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 mbar_arrive_expect_tx(&full_bar[i], S::STAGE_BYTES);
                 load_a<KIND>(smem + i * S::STAGE_BYTES, &tmA0, &tmA1, &tmA2, &full_bar[i], a, tile, (kb0 + i) * 64,
                              pol_w);
+            }
+            if constexpr (KIND != EPI_LMHEAD) {
+                const int ahead = min(nk, pre + kL2AheadBlocks);
+                for (int i = pre; i < ahead; ++i) prefetch_a<KIND>(&tmA0, &tmA1, &tmA2, a, tile, (kb0 + i) * 64);
             }
             pdl_wait();  // activations come from the previous kernel
             for (int i = 0; i < pre; ++i)
@@ -394,7 +362,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     int R = 0;
     if (warp < 4) {
-        // ---------------- epilogue warps 0-3: rstd rows, then the accumulator
+        // ---------------- epilogue warps 0-3: rstd rows, then the accumulator into shared memory
         pdl_wait();
         R = *a.nrows;
         if (R > N) {
@@ -412,50 +380,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 es.rstd[r] = s;
             }
         }
-        named_bar_sync(1, 128);
         if (!mbar_wait(&accum_bar, 0)) set_status(a.status, SDV_ERR_DEVICE_TIMEOUT);
         tc_fence_after();
         const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const int f = threadIdx.x;
         float v[32];
+        for (int c0 = 0; c0 < R; c0 += 32) {
+            tmem_ld32(taddr + c0, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (c0 + j < R) red[(c0 + j) * 128 + f] = v[j];
+        }
+    }
+    // every partial of the tile is parked in shared memory (of each CTA of the cluster)
+    if (clustered) cluster_sync();
+    else if (warp < 4) named_bar_sync(1, 128);
+    if (warp < 4) {
+        int s0 = 0, s1 = R;
         if (clustered) {
-            const int f = threadIdx.x;
-            for (int c0 = 0; c0 < R; c0 += 32) {
-                tmem_ld32(taddr + c0, v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c0 + j < R) red[(c0 + j) * 128 + f] = v[j];
-            }
-        } else {
-            for (int c0 = 0; c0 < R; c0 += 32) {
-                tmem_ld32(taddr + c0, v);
-                epi_dispatch<KIND>(a, es, xch, tile, c0, R, v);
-            }
-        }
-    }
-    if (clustered) {
-        // every partial of the tile is parked in its CTA's shared memory
-        cluster_sync();
-        if (warp < 4) {
-            const int f = threadIdx.x;
             const int per = (R + a.splits - 1) / a.splits;
-            const int s0 = min(R, static_cast<int>(cluster_ctarank()) * per), s1 = min(R, s0 + per);
-            const uint32_t red_local = smem_u32(red);
-            float v[32];
-            for (int c0 = s0; c0 < s1; c0 += 32) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.f;
-                for (int q = 0; q < a.splits; ++q) {  // fixed split order
-                    const uint32_t base = mapa_shared(red_local, static_cast<uint32_t>(q));
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (c0 + j < s1) v[j] += ld_dsmem(base + static_cast<uint32_t>(((c0 + j) * 128 + f) * 4));
-                }
-                epi_dispatch<KIND>(a, es, xch, tile, c0, s1, v);
-            }
+            s0 = min(R, static_cast<int>(cluster_ctarank()) * per);
+            s1 = min(R, s0 + per);
         }
-        // no CTA leaves while its partial may still be read
-        cluster_sync();
+        const uint32_t red_local = smem_u32(red);
+        for (int r = s0 + warp; r < s1; r += 4) {
+            float x[4];
+            if (clustered) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) x[i] = 0.f;
+                for (int q = 0; q < a.splits; ++q) {  // fixed split order
+                    const uint32_t base = mapa_shared(red_local, static_cast<uint32_t>(q)) + r * 512 + lane * 4;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) x[i] += ld_dsmem(base + 128 * i);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) x[i] = red[r * 128 + lane + 32 * i];
+            }
+            epi_row<KIND>(a, es, tile, r, lane, x);
+        }
     }
+    if (clustered) cluster_sync();  // no CTA leaves while its partial may still be read
     if constexpr (KIND == EPI_LMHEAD) {
         if (warp < 4) {
             __threadfence();

@@ -26,7 +26,6 @@ struct GemmPlan {
 };
 
 constexpr int kRowsCap = 128;     // activation rows held in the workspace (max_rows <= 128)
-constexpr int kAttnChunk = 256;   // keys per attention work item
 constexpr int kNs[4] = {16, 32, 64, 128};
 
 int n_index(int max_rows) {
@@ -78,6 +77,7 @@ struct sdv_ctx {
     std::vector<float2> rope_host;
     float *attn_po = nullptr;
     float2 *attn_pml = nullptr;
+    int *attn_cnt = nullptr;
     int ss_tiles = 0, grp = 0, qrows = 0, work_cap = 0, pages_per_seq = 0, ng_slots = 0;
     size_t layer_stride = 0;  // pool elements per layer
     GemmPlan plan[5];         // qkv, o, gate/up, down, lm head
@@ -149,7 +149,7 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     const int pps = ceil_div(c.max_context, c.page_size);
     const int grp = m.n_q_heads / m.n_kv_heads;
     const int qrows = 128 / grp;
-    const int work_cap = ceil_div(static_cast<long long>(c.n_pages) * c.page_size, kAttnChunk) + B;
+    const int work_cap = ceil_div(static_cast<long long>(c.n_pages) * c.page_size, kAttnGroup) + B;
     const int ng_slots = c.ngram_capacity > 0 ? next_pow2(std::max(16, 2 * c.ngram_capacity)) : 0;
     const int ss_tiles = ceil_div(H, 128);
 
@@ -211,6 +211,7 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     const size_t nslots = static_cast<size_t>(work_cap) * m.n_kv_heads * grp * qrows;
     float *apo = reinterpret_cast<float *>(take(sizeof(float) * nslots * D));
     float2 *apml = reinterpret_cast<float2 *>(take(sizeof(float2) * nslots));
+    int *acnt = reinterpret_cast<int *>(take(sizeof(int) * static_cast<size_t>(B) * m.n_kv_heads * kAttnCluster));
 
     if (ctx) {
         ctx->st = s;
@@ -230,6 +231,7 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
         ctx->rope = rope;
         ctx->attn_po = apo;
         ctx->attn_pml = apml;
+        ctx->attn_cnt = acnt;
         ctx->ss_tiles = ss_tiles;
         ctx->grp = grp;
         ctx->qrows = qrows;
@@ -250,7 +252,7 @@ int check_cfg(const sdv_model_cfg *m, const sdv_cache_cfg *c) {
     const int grp = m->n_q_heads / m->n_kv_heads;
     if (grp > 8 || 128 % grp) return SDV_ERR_UNSUPPORTED;
     if ((m->n_q_heads * m->head_dim) % 128 || (m->n_kv_heads * m->head_dim) % 128) return SDV_ERR_UNSUPPORTED;
-    if (m->hidden % 8 || m->ffn % 8 || m->vocab >= (1 << 30)) return SDV_ERR_UNSUPPORTED;
+    if (m->hidden % 8 || m->ffn % 8 || m->hidden > 8192 || m->vocab >= (1 << 30)) return SDV_ERR_UNSUPPORTED;
     if (c->page_size <= 0 || c->n_pages <= 0 || c->max_batch <= 0 || c->max_batch > 256) return SDV_ERR_ARG;
     if (c->max_rows <= 0 || c->max_rows > kRowsCap || c->max_span <= 0 || c->max_span > c->max_rows)
         return SDV_ERR_ARG;
@@ -297,6 +299,31 @@ cudaError_t launch(const sdv_ctx *ctx, void (*kern)(KArgs...), dim3 grid, dim3 b
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = ctx->use_pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster(const sdv_ctx *ctx, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t st, int cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (ctx->use_pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster_x;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
@@ -349,19 +376,22 @@ cudaError_t launch_gemm(const sdv_ctx *ctx, int nidx, const CUtensorMap &a0, con
     }
 }
 
+// Dynamic shared memory for a kernel, and the largest shared-memory carveout so that two
+// CTAs fit on an SM (the default carveout leaves room for one).
+template <typename K>
+cudaError_t set_smem(K kern, int bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    return e;
+}
+
 template <int N>
 cudaError_t set_gemm_smem() {
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<N, EPI_QKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         GemmShape<N>::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm_kernel<N, EPI_RESID>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GemmShape<N>::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm_kernel<N, EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GemmShape<N>::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(gemm_kernel<N, EPI_LMHEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 GemmShape<N>::SMEM_BYTES);
+    cudaError_t e = set_smem(gemm_kernel<N, EPI_QKV>, GemmShape<N>::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(gemm_kernel<N, EPI_RESID>, GemmShape<N>::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(gemm_kernel<N, EPI_SWIGLU>, GemmShape<N>::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(gemm_kernel<N, EPI_LMHEAD>, GemmShape<N>::SMEM_BYTES);
     return e;
 }
 
@@ -390,6 +420,7 @@ GemmArgs base_args(const sdv_ctx *ctx, int kind, int pidx) {
 
 // Paged attention of `layer` over the rows prepared in the device state.
 int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, bf16 *out, int max_rows, int max_span, cudaStream_t st) {
+    (void)max_rows;
     const sdv_model_cfg &m = ctx->m;
     AttnArgs a{};
     a.q = q;
@@ -401,32 +432,28 @@ int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, bf16 *out, int max_row
     a.seq_base = ctx->st.seq_base;
     a.row_off = ctx->st.row_off;
     a.work = ctx->st.work;
-    a.work_off = ctx->st.work_off;
     a.n_work = ctx->st.n_work;
-    a.row_seq = ctx->st.row_seq;
-    a.nrows = ctx->st.nrows;
     a.nq = m.n_q_heads;
     a.nkv = m.n_kv_heads;
     a.D = m.head_dim;
     a.grp = ctx->grp;
-    a.chunk = kAttnChunk;
     a.qrows = ctx->qrows;
     a.scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(m.head_dim));
     a.part_o = ctx->attn_po;
     a.part_ml = ctx->attn_pml;
+    a.counters = ctx->attn_cnt;
     a.out = out;
     a.status = ctx->st.status;
+    const dim3 grid(ctx->work_cap * kAttnCluster, m.n_kv_heads);
     for (int q0 = 0; q0 < max_span; q0 += ctx->qrows) {
         a.q0 = q0;
         cudaError_t e;
         if (m.head_dim == 128)
-            e = launch(ctx, attn_partial_kernel<128>, dim3(ctx->work_cap, m.n_kv_heads), dim3(kAttnThreads),
-                       AttnShape<128>::SMEM, st, a);
+            e = launch_cluster(ctx, attn_kernel<128>, grid, dim3(kAttnThreads), AttnShape<128>::SMEM, st,
+                               kAttnCluster, a);
         else
-            e = launch(ctx, attn_partial_kernel<64>, dim3(ctx->work_cap, m.n_kv_heads), dim3(kAttnThreads),
-                       AttnShape<64>::SMEM, st, a);
-        if (e != cudaSuccess) return SDV_ERR_CUDA;
-        e = launch(ctx, attn_combine_kernel, dim3(max_rows, m.n_kv_heads), dim3(m.head_dim), 0, st, a);
+            e = launch_cluster(ctx, attn_kernel<64>, grid, dim3(kAttnThreads), AttnShape<64>::SMEM, st,
+                               kAttnCluster, a);
         if (e != cudaSuccess) return SDV_ERR_CUDA;
     }
     return SDV_OK;
@@ -442,7 +469,7 @@ int prepare(sdv_ctx *ctx, const int32_t *tokens, const int32_t *row_off, const i
     p.B = B;
     p.max_rows = max_rows;
     p.max_span = max_span;
-    p.chunk = kAttnChunk;
+    p.chunk = kAttnGroup;
     p.embed = embed;
     p.E = static_cast<const bf16 *>(ctx->w.embed);
     p.g0 = static_cast<const bf16 *>(ctx->layers[0].attn_norm);
@@ -556,8 +583,8 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
     if (e == cudaSuccess) e = set_gemm_smem<32>();
     if (e == cudaSuccess) e = set_gemm_smem<64>();
     if (e == cudaSuccess) e = set_gemm_smem<128>();
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_partial_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnShape<128>::SMEM);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(attn_partial_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnShape<64>::SMEM);
+    if (e == cudaSuccess) e = set_smem(attn_kernel<128>, AttnShape<128>::SMEM);
+    if (e == cudaSuccess) e = set_smem(attn_kernel<64>, AttnShape<64>::SMEM);
     if (e != cudaSuccess) {
         delete ctx;
         return SDV_ERR_CUDA;

@@ -157,23 +157,32 @@ __global__ void prepare_kernel(PrepArgs p) {
         set_status(s.status, SDV_ERR_DEVICE);
         tok = 0;
     }
-    __shared__ float red[4];
+    // every load first (independent), then the per-128-feature sums of squares
+    __shared__ float red[4][64];
     const bf16 *e = p.E + static_cast<size_t>(tok) * p.H;
     const int ntile = (p.H + 127) / 128;
-    for (int t = 0; t < ntile; ++t) {
+    constexpr int kMaxTiles = 64;  // hidden <= 8192
+    float vals[kMaxTiles];
+#pragma unroll
+    for (int t = 0; t < kMaxTiles; ++t) {
         const int f = t * 128 + threadIdx.x;
-        float v = 0.f;
-        if (f < p.H) {
-            v = __bfloat162float(e[f]);
-            p.x[static_cast<size_t>(r) * p.H + f] = v;
-            p.xb[static_cast<size_t>(r) * p.H + f] = __float2bfloat16(v * __bfloat162float(p.g0[f]));
-        }
-        float sq = warp_sum(v * v);
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sq;
-        __syncthreads();
-        if (threadIdx.x == 0) p.ss[static_cast<size_t>(t) * p.rows_cap + r] = (red[0] + red[1]) + (red[2] + red[3]);
-        __syncthreads();
+        vals[t] = (t < ntile && f < p.H) ? __bfloat162float(e[f]) : 0.f;
     }
+#pragma unroll
+    for (int t = 0; t < kMaxTiles; ++t) {
+        const int f = t * 128 + threadIdx.x;
+        if (t < ntile && f < p.H) {
+            p.x[static_cast<size_t>(r) * p.H + f] = vals[t];
+            p.xb[static_cast<size_t>(r) * p.H + f] = __float2bfloat16(vals[t] * __bfloat162float(p.g0[f]));
+        }
+        if (t < ntile) {
+            const float sq = warp_sum(vals[t] * vals[t]);
+            if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5][t] = sq;
+        }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < ntile; t += blockDim.x)
+        p.ss[static_cast<size_t>(t) * p.rows_cap + r] = (red[0][t] + red[1][t]) + (red[2][t] + red[3][t]);
 }
 
 // ------------------------------------------------------------------ accept
