@@ -238,6 +238,34 @@ int sdv_profile_enable(sdv_ctx *ctx, int on);
  * recorded group into h_ms[7] and h_count[7], and clear the record. */
 int sdv_profile_read(sdv_ctx *ctx, float *h_ms, int32_t *h_count);
 
+/* Paged attention without any device allocation, for callers that cannot
+ * call cudaMalloc: code running while a CUDA graph is being captured,
+ * plug-in interfaces that are handed only their input and output buffers,
+ * and deployments whose device memory is fixed at start-up. The pages have
+ * no counterpart of this call; it is a variant of sdv_op_attention that needs
+ * neither a context nor a workspace.
+ *   Inputs: d_q [R][n_q_heads][head_dim] bf16 (after RoPE); d_kv_layer, one
+ *   layer of a KV pool laid out as in sdv_kv_pool_bytes ([n_pages][2][n_kv_heads]
+ *   [page_size][head_dim] bf16); d_page_table [B][pages_per_seq] int32;
+ *   d_row_off [B+1] and d_base [B] as in sdv_op_attention. Output: d_out
+ *   [R][n_q_heads*head_dim] bf16.
+ *   Scratch: a file-scope device array of 8 MiB, held by every GPU that loads
+ *   the library until the process exits. The first call on a device resolves
+ *   that array's device address and sets kernel attributes; make that first
+ *   call before any stream capture. All calls share the array, so calls that
+ *   overlap on the GPU race (calls on different devices do not share it); group counters are cleared on every call.
+ *   Limits: B <= 64, head_dim 64 or 128, every L_b + S_b <= max_context <=
+ *   pages_per_seq * page_size, and the scratch the shapes need (about
+ *   B * ceil(max_context/1024) * n_kv_heads * n_q_heads/n_kv_heads *
+ *   min(max_span, 128*n_kv_heads/n_q_heads) * (4*head_dim + 8) bytes) within
+ *   8 MiB; beyond it the call returns SDV_ERR_CAPACITY and enqueues nothing.
+ *   A sequence whose span passes max_context gets NaN rows. No device memory
+ *   is allocated or freed. */
+int sdv_paged_attention_noalloc(const void *d_q, const void *d_kv_layer, const int32_t *d_page_table,
+                                int pages_per_seq, int page_size, int n_pages, const int32_t *d_row_off,
+                                const int32_t *d_base, int B, int n_q_heads, int n_kv_heads, int head_dim,
+                                int max_span, int max_context, void *d_out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,7 @@ EXPORTS = (
     "sdv_workspace_bytes", "sdv_kv_pool_bytes", "sdv_create", "sdv_destroy", "sdv_ensure_capacity",
     "sdv_spec_forward", "sdv_accept_greedy", "sdv_rewind_cache", "sdv_cache_seq_len", "sdv_page_table",
     "sdv_ngram_commit", "sdv_gen_init", "sdv_propose", "sdv_reset_seq", "sdv_get_status", "sdv_status_str",
-    "sdv_op_attention", "sdv_profile_enable", "sdv_profile_read",
+    "sdv_op_attention", "sdv_profile_enable", "sdv_profile_read", "sdv_paged_attention_noalloc",
 )
 PHASES = ("prepare", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm")
 
@@ -99,6 +99,7 @@ def lib():
     L.sdv_op_attention.argtypes = [vp, i32, vp, vp, vp, i32, i32, vp, vp]
     L.sdv_profile_enable.argtypes = [vp, i32]
     L.sdv_profile_read.argtypes = [vp, P(ctypes.c_float), P(ctypes.c_int32)]
+    L.sdv_paged_attention_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
     for name in EXPORTS:
         if name != "sdv_status_str":
             getattr(L, name).restype = i32
@@ -140,6 +141,15 @@ def _stream(stream) -> int:
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return int(s.cuda_stream)
+
+
+def paged_attention_noalloc(q, kv_layer, page_table, pages_per_seq, page_size, n_pages, row_off, base, B,
+                            n_q_heads, n_kv_heads, head_dim, max_span, max_context, out, stream=None):
+    """Paged attention with no device allocation (scratch in a static device array)."""
+    _check(lib().sdv_paged_attention_noalloc(_ptr(q), _ptr(kv_layer), _ptr(page_table), pages_per_seq, page_size,
+                                             n_pages, _ptr(row_off), _ptr(base), B, n_q_heads, n_kv_heads, head_dim,
+                                             max_span, max_context, _ptr(out), _stream(stream)),
+           "paged_attention_noalloc")
 
 
 def upload_bf16(bits: np.ndarray, device="cuda"):
