@@ -25,7 +25,7 @@ struct AttnArgs {
     int pages_per_seq, page_size, n_pages;
     const int *seq_base;     // [B] cache length before the span
     const int *row_off;      // [B+1]
-    const int *work;         // [n] (b << 16) | group
+    const int4 *work;        // [n] (b | group << 16, L_b, S_b, first row of b)
     const int *n_work;       // [1]
     int nq, nkv, D, grp;
     int q0, qrows;           // span rows q0 .. q0+qrows-1 handled by this launch
@@ -110,10 +110,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs a)
     const int cr = static_cast<int>(cluster_ctarank());
     // Both early exits depend only on (w, b), which the 8 CTAs of a cluster share,
     // so a cluster leaves whole and never waits on a departed CTA.
+    const int4 wi = a.work[w];  // (the list has room for every CTA's index; stale past n_work)
     if (w >= *a.n_work) return;
-    const int b = a.work[w] >> 16, grp_idx = a.work[w] & 0xffff;
-    const int L = a.seq_base[b];
-    const int S_b = a.row_off[b + 1] - a.row_off[b];
+    const int b = wi.x & 0xffff, grp_idx = wi.x >> 16;
+    const int L = wi.y, S_b = wi.z, row0 = wi.w;
     const int ni = max(0, min(S_b - a.q0, a.qrows));
     if (ni == 0) return;
     const int M = a.grp * ni;
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs a)
             const bool valid = j < M;
             const bf16 *src = a.q;
             if (valid) {
-                const int r = a.row_off[b] + a.q0 + j / a.grp;
+                const int r = row0 + a.q0 + j / a.grp;
                 const int h = g * a.grp + j % a.grp;
                 src = a.q + (static_cast<size_t>(r) * a.nq + h) * D + ch * 8;
             }
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs a)
             den += sc * ld_dsmem_rank(&ml_s[j].y, static_cast<uint32_t>(q));
             num += sc * ld_dsmem_rank(&po_s[j * D + d], static_cast<uint32_t>(q));
         }
-        const int r = a.row_off[b] + a.q0 + j / a.grp;
+        const int r = row0 + a.q0 + j / a.grp;
         const int h = g * a.grp + j % a.grp;
         if (n_groups == 1) {
             a.out[(static_cast<size_t>(r) * a.nq + h) * D + d] = __float2bfloat16(num / den);
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_kernel(const AttnArgs a)
                     den += sc * ml.y;
                     num += sc * __ldcg(&a.part_o[sl * D + d]);
                 }
-                const int r = a.row_off[b] + a.q0 + j / a.grp;
+                const int r = row0 + a.q0 + j / a.grp;
                 const int h = g * a.grp + j % a.grp;
                 a.out[(static_cast<size_t>(r) * a.nq + h) * D + d] = __float2bfloat16(num / den);
             }

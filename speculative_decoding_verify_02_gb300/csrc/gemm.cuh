@@ -23,6 +23,7 @@ enum EpiKind : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LMHEAD = 3 
 struct GemmArgs {
     int kind;
     int tiles, splits, kps, k_blocks;  // output tiles, K splits, k-blocks per split, total k-blocks (64 wide)
+    int l2_ahead;                      // k-blocks prefetched into L2 beyond the shared-memory stages
     int n_out;                         // valid output features (ffn for SwiGLU)
     int rows_cap;                      // row stride of partial / ss buffers
     const int *nrows;                  // device: rows present (R)
@@ -257,9 +258,6 @@ __device__ __forceinline__ void prefetch_a(const CUtensorMap *tmA0, const CUtens
     }
 }
 
-// k-blocks of weights each CTA pulls into L2 ahead of its pipeline before waiting on the
-// previous kernel (none for the LM head, whose 778 MB would only thrash L2)
-constexpr int kL2AheadBlocks = 16;
 
 template <int N, int KIND>
 __global__ void __launch_bounds__(kGemmThreads, 2)
@@ -318,10 +316,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 load_a<KIND>(smem + i * S::STAGE_BYTES, &tmA0, &tmA1, &tmA2, &full_bar[i], a, tile, (kb0 + i) * 64,
                              pol_w);
             }
-            if constexpr (KIND != EPI_LMHEAD) {
-                const int ahead = min(nk, pre + kL2AheadBlocks);
-                for (int i = pre; i < ahead; ++i) prefetch_a<KIND>(&tmA0, &tmA1, &tmA2, a, tile, (kb0 + i) * 64);
-            }
+            // optionally pull further weight tiles into L2 while the previous kernel runs
+            const int ahead = min(nk, pre + a.l2_ahead);
+            for (int i = pre; i < ahead; ++i) prefetch_a<KIND>(&tmA0, &tmA1, &tmA2, a, tile, (kb0 + i) * 64);
             pdl_wait();  // activations come from the previous kernel
             for (int i = 0; i < pre; ++i)
                 tma_load_2d(smem + i * S::STAGE_BYTES + S::A_BYTES, &tmB, &full_bar[i], (kb0 + i) * 64, 0);

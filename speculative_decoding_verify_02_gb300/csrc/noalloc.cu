@@ -43,7 +43,7 @@ Layout layout(int B, int nkv, int D, int rows_per_item, int max_work) {
     Layout L;
     size_t off = 256;
     L.work = off;
-    off = up256(off + sizeof(int) * static_cast<size_t>(max_work));
+    off = up256(off + sizeof(int4) * static_cast<size_t>(max_work));
     L.counters = off;
     off = up256(off + sizeof(int) * static_cast<size_t>(B) * nkv * kAttnCluster);
     L.ml = off;
@@ -58,7 +58,7 @@ Layout layout(int B, int nkv, int D, int rows_per_item, int max_work) {
 // with a span), zeroed group counters, and NaN rows for any sequence whose
 // span passes max_context (it gets no work).
 __global__ void noalloc_prep_kernel(const int *row_off, const int *base, int B, int nkv, int max_context, int max_work,
-                                    int *status, int *n_work, int *work, int *counters, bf16 *out, int row_elems) {
+                                    int *status, int *n_work, int4 *work, int *counters, bf16 *out, int row_elems) {
     pdl_wait();
     __shared__ int off_s[65];
     for (int i = threadIdx.x; i < B * nkv * kAttnCluster; i += blockDim.x) counters[i] = 0;
@@ -85,8 +85,8 @@ __global__ void noalloc_prep_kernel(const int *row_off, const int *base, int B, 
     __syncthreads();
     for (int b = 0; b < B; ++b) {
         const int n = off_s[b + 1] - off_s[b];
-        for (int g = threadIdx.x; g < n; g += blockDim.x) work[off_s[b] + g] = (b << 16) | g;
         const int S = row_off[b + 1] - row_off[b];
+        for (int g = threadIdx.x; g < n; g += blockDim.x) work[off_s[b] + g] = make_int4(b | (g << 16), base[b], S, row_off[b]);
         if (S > 0 && n == 0) {  // rejected sequence: its rows read as NaN rather than stale memory
             const size_t e0 = static_cast<size_t>(row_off[b]) * row_elems, e1 = static_cast<size_t>(row_off[b + 1]) * row_elems;
             for (size_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) out[e] = __float2bfloat16(NAN);
@@ -163,7 +163,7 @@ extern "C" int sdv_paged_attention_noalloc(const void *d_q, const void *d_kv_lay
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int *status = reinterpret_cast<int *>(scratch);
     int *n_work = status + 1;
-    int *work = reinterpret_cast<int *>(scratch + L.work);
+    int4 *work = reinterpret_cast<int4 *>(scratch + L.work);
     int *counters = reinterpret_cast<int *>(scratch + L.counters);
     noalloc_prep_kernel<<<1, 256, 0, st>>>(d_row_off, d_base, B, n_kv_heads, max_context, max_work, status, n_work,
                                             work, counters, static_cast<bf16 *>(d_out), n_q_heads * head_dim);

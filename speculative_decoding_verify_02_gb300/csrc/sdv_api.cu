@@ -171,7 +171,7 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     s.row_off = reinterpret_cast<int *>(take(sizeof(int) * (B + 1)));
     s.row_seq = reinterpret_cast<int *>(take(sizeof(int) * kRowsCap));
     s.row_pos = reinterpret_cast<int *>(take(sizeof(int) * kRowsCap));
-    s.work = reinterpret_cast<int *>(take(sizeof(int) * static_cast<size_t>(work_cap)));
+    s.work = reinterpret_cast<int4 *>(take(sizeof(int4) * static_cast<size_t>(work_cap)));
     s.work_off = reinterpret_cast<int *>(take(sizeof(int) * (B + 1)));
     s.n_work = reinterpret_cast<int *>(take(sizeof(int)));
     s.hist = reinterpret_cast<int *>(take(sizeof(int) * static_cast<size_t>(B) * std::max(0, c.ngram_capacity)));
@@ -678,8 +678,10 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
             r = run_attention(ctx, l, ctx->q, ctx->attn_o, max_rows, max_span, st);
         }
         if (r) return r;
-        // O projection + residual; emits bf16(x * g_ffn) and sum-of-squares parts
+        // O projection + residual; emits bf16(x * g_ffn) and sum-of-squares parts. Its weights
+        // (21 MB) are pulled into L2 during the attention, when HBM is otherwise idle.
         a = base_args(ctx, EPI_RESID, P_O);
+        a.l2_ahead = 64;
         a.n_out = m.hidden;
         a.x = ctx->x;
         a.xb = ctx->xb;

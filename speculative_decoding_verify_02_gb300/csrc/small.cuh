@@ -20,7 +20,7 @@ struct DevState {
     int *row_off;       // [max_batch+1] copy of the current forward's offsets
     int *row_seq;       // [rows_cap]
     int *row_pos;       // [rows_cap]
-    int *work;          // attention work list
+    int4 *work;         // attention work list: (b | group << 16, L_b, S_b, first row of b)
     int *work_off;      // [max_batch+1]
     int *n_work;        // [1]
     // n-gram / loop state
@@ -144,7 +144,10 @@ __global__ void prepare_kernel(PrepArgs p) {
         }
         for (int b = 0; b < p.B; ++b) {
             const int w0 = wo_s[b], n = wo_s[b + 1] - w0;
-            for (int c = threadIdx.x; c < n; c += blockDim.x) s.work[w0 + c] = (b << 16) | c;
+            if (n == 0) continue;
+            const int L = p.base ? p.base[b] : s.seq_base[b];
+            const int r0 = p.row_off[b], S = p.row_off[b + 1] - r0;
+            for (int c = threadIdx.x; c < n; c += blockDim.x) s.work[w0 + c] = make_int4(b | (c << 16), L, S, r0);
         }
         for (int r = threadIdx.x; r < p.rows_cap; r += blockDim.x) p.keys[r] = 0ull;
         return;
