@@ -27,12 +27,12 @@ invariants the pages state. Parity of the decoder's logits is pinned by those
 library cross-checks and invariants only; the pages print no logits that could
 pin values for these synthetic models.
 """
-from .model import DenseDecoder, SeqCache, rmsnorm, silu, rope_neox, attention_rows, argmax_lowest
+from .model import DenseDecoder, SeqCache, rmsnorm, silu, rope_neox, attention_rows, argmax_lowest, round_bf16
 from .pages import PagePool, CapacityError
 from .spec import accept_greedy, ngram_propose, adapt_k
 from .loop import generate, StepRecord
 
 __all__ = [
-    "DenseDecoder", "SeqCache", "rmsnorm", "silu", "rope_neox", "attention_rows", "argmax_lowest",
+    "DenseDecoder", "SeqCache", "round_bf16", "rmsnorm", "silu", "rope_neox", "attention_rows", "argmax_lowest",
     "PagePool", "CapacityError", "accept_greedy", "ngram_propose", "adapt_k", "generate", "StepRecord",
 ]

@@ -45,7 +45,8 @@ class StepRecord:
 
 def generate(model, prompts, n_tokens: int, drafter: str = "ngram", k: int = 4, adaptive: bool = False,
              k_max: int = 7, ngram_n: int = 2, tables=None, page_size: int = 16, n_pages: int = None,
-             max_pages_per_seq: int = None, prefill_chunk: int = 128, keep_logits: bool = False):
+             max_pages_per_seq: int = None, prefill_chunk: int = 128, keep_logits: bool = False,
+             kv_dtype: str = "f64"):
     """Run the loop for every sequence until each has n_tokens generated tokens.
 
     drafter: "ngram" (prompt lookup over the sequence's history), "table"
@@ -59,7 +60,7 @@ def generate(model, prompts, n_tokens: int, drafter: str = "ngram", k: int = 4, 
         max_pages_per_seq = -(-cap // page_size)
     if n_pages is None:
         n_pages = B * max_pages_per_seq
-    caches = [SeqCache(sh, cap) for _ in range(B)]
+    caches = [SeqCache(sh, cap, kv_dtype) for _ in range(B)]
     pool = PagePool(n_pages, page_size, B, max_pages_per_seq)
 
     last_logits = []
@@ -73,7 +74,7 @@ def generate(model, prompts, n_tokens: int, drafter: str = "ngram", k: int = 4, 
             pool.ensure_capacity(req)
             spans = [[] for _ in range(B)]
             spans[b] = chunk
-            lg = model.forward(caches, spans)[b]
+            lg = model.forward(caches, spans, last_row_logits=True)[b]
             pool.set_length(b, caches[b].length)
         last_logits.append(lg[-1])
     first = [int(argmax_lowest(v)) for v in last_logits]

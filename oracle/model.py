@@ -29,6 +29,17 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest bf16 value (ties to even), returned as float64.
+
+    The value is first rounded to float32 (nearest even), then its low 16 bits
+    are rounded away: add 0x7FFF plus the lowest kept bit, truncate.
+    """
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16 << 16
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
     """x / sqrt(mean(x^2) + eps) * g over the last axis."""
     ms = np.mean(x * x, axis=-1, keepdims=True)
@@ -90,13 +101,25 @@ class SeqCache:
 
     Positions at or beyond ``length`` may hold stale rows from a rejected
     verify; nothing reads them before the next forward overwrites them.
+
+    kv_dtype is the storage precision of the cache: "f64" keeps K/V exactly;
+    "bf16" stores them rounded to bf16, as the bf16 KV cache of the bf16
+    target models on the pages does (pegainfer's Qwen3-4B runs in bf16).
     """
 
-    def __init__(self, shape, capacity: int):
+    def __init__(self, shape, capacity: int, kv_dtype: str = "f64"):
+        assert kv_dtype in ("f64", "bf16")
         self.K = [np.zeros((capacity, shape.n_kv_heads, shape.head_dim)) for _ in range(shape.n_layers)]
         self.V = [np.zeros((capacity, shape.n_kv_heads, shape.head_dim)) for _ in range(shape.n_layers)]
         self.length = 0
         self.capacity = capacity
+        self.kv_dtype = kv_dtype
+
+    def store(self, l: int, at: int, k: np.ndarray, v: np.ndarray) -> None:
+        if self.kv_dtype == "bf16":
+            k, v = round_bf16(k), round_bf16(v)
+        self.K[l][at:at + len(k)] = k
+        self.V[l][at:at + len(v)] = v
 
 
 class DenseDecoder:
@@ -118,16 +141,17 @@ class DenseDecoder:
         return t
 
     def embed(self, toks: np.ndarray) -> np.ndarray:
-        if self._cache is not None:
-            return self.w("embed")[toks]
+        # only the gathered rows are converted
         return bf16_to_f64(self._fn("embed")[toks])
 
-    def forward(self, caches: list, spans: list, keep_hidden: bool = False):
+    def forward(self, caches: list, spans: list, keep_hidden: bool = False, last_row_logits: bool = False):
         """One forward over span b of every sequence b (spans may be empty).
 
         Rows of sequence b sit at positions caches[b].length + i. Every row's
         K/V is written before any row attends; afterwards each cache length
-        grows by its span length. Returns per-sequence logits [S_b, V].
+        grows by its span length. Returns per-sequence logits [S_b, V]; with
+        last_row_logits only the last row of each span gets logits ([1, V]),
+        the others are not computed.
         """
         sh = self.shape
         eps, D, nq, nkv = sh.rms_eps, sh.head_dim, sh.n_q_heads, sh.n_kv_heads
@@ -156,8 +180,7 @@ class DenseDecoder:
             k = rope_neox(k, pos[:, None], sh.rope_theta)
             for b, c in enumerate(counts):                            # K/V of every row first
                 L0, r0 = caches[b].length, starts[b]
-                caches[b].K[l][L0:L0 + c] = k[r0:r0 + c]
-                caches[b].V[l][L0:L0 + c] = v[r0:r0 + c]
+                caches[b].store(l, L0, k[r0:r0 + c], v[r0:r0 + c])
             o = np.empty((R, nq, D))
             for b, c in enumerate(counts):
                 if c == 0:
@@ -170,9 +193,20 @@ class DenseDecoder:
             f = silu(hb @ self.w(p + "w_gate").T) * (hb @ self.w(p + "w_up").T)
             x = x + f @ self.w(p + "w_down").T
         y = rmsnorm(x, self.w("final_norm"), eps)
-        logits = y @ self.w("lm_head").T                               # [R, V]
         for b, c in enumerate(counts):
             caches[b].length += c
+        if last_row_logits:
+            last = [starts[b + 1] - 1 for b in range(len(spans)) if counts[b] > 0]
+            lg = y[last] @ self.w("lm_head").T
+            out, k = [], 0
+            for b in range(len(spans)):
+                if counts[b] > 0:
+                    out.append(lg[k:k + 1])
+                    k += 1
+                else:
+                    out.append(np.zeros((0, sh.vocab)))
+            return (out, y) if keep_hidden else out
+        logits = y @ self.w("lm_head").T                               # [R, V]
         out = [logits[starts[b]:starts[b + 1]] for b in range(len(spans))]
         if keep_hidden:
             return out, y

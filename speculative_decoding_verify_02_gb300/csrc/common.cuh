@@ -70,7 +70,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, ui
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
         : "memory");
 }
-// Same, with an L2 eviction-priority hint (createpolicy result).
+// 3-D tiled bulk copy global -> shared (used for an activation's hi/lo planes in one box).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+// Same as tma_load_2d, with an L2 eviction-priority hint (createpolicy result).
 __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1,
                                                  uint64_t policy) {
     asm volatile(
@@ -171,6 +179,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 }
 
 // ------------------------------------------------------------------ small helpers
+// An fp32 activation as a pair of bf16 values, hi = bf16(x) and lo = bf16(x - hi):
+// x is recovered to about 16 significant bits, and a bf16 tensor-core product
+// with an exact bf16 operand keeps that precision when both halves are applied.
+struct Bf16Pair {
+    bf16 hi, lo;
+};
+__device__ __forceinline__ Bf16Pair split_bf16(float x) {
+    Bf16Pair p;
+    p.hi = __float2bfloat16(x);
+    p.lo = __float2bfloat16(x - __bfloat162float(p.hi));
+    return p;
+}
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -4,7 +4,9 @@
 // The verify span has few rows (K+1 per sequence, <= 128 in all), so the weight
 // matrix is the tcgen05 A operand (M = 128 output features per tile, streamed
 // from HBM by TMA with 128-byte swizzle) and the activations are the B operand
-// (N = rows padded to 16/32/64/128, read from L2). The accumulator sits in
+// (N = rows padded to 16/32/64/128, read from L2), held as a bf16 hi/lo pair
+// applied by two MMAs, so activations keep about 16 significant bits while
+// the weights stay exactly bf16. The accumulator sits in
 // TMEM. Warp roles: warp 4 issues TMA, warp 5 issues MMAs, warps 0-3 run the
 // epilogue from tcgen05.ld. When K is split, the splits of one tile form a
 // thread-block cluster: each CTA parks its fp32 partial in its own shared
@@ -25,7 +27,7 @@ struct GemmArgs {
     int tiles, splits, kps, k_blocks;  // output tiles, K splits, k-blocks per split, total k-blocks (64 wide)
     int l2_ahead;                      // k-blocks prefetched into L2 beyond the shared-memory stages
     int n_out;                         // valid output features (ffn for SwiGLU)
-    int rows_cap;                      // row stride of partial / ss buffers
+    int rows_cap;                      // rows of the activation / ss buffers (plane stride in rows)
     const int *nrows;                  // device: rows present (R)
     int *status;
     // rstd of the RMSNorm feeding this GEMM (QKV, SwiGLU, LM head): from sum-of-squares parts
@@ -43,14 +45,14 @@ struct GemmArgs {
     int rope_rows;
     const int *row_seq, *row_pos, *page_table;
     int pages_per_seq, page_size, n_pages;
-    bf16 *q_out, *kv_layer;
+    bf16 *q_out, *kv_layer;            // q_out: [2 planes][rows_cap][nq][D]
     // residual epilogue
     float *x;
-    bf16 *xb;
+    bf16 *xb;                          // [2 planes][rows_cap][hidden]
     const bf16 *g_next;
     float *ss_out;
     // SwiGLU epilogue
-    bf16 *h_out;
+    bf16 *h_out;                       // [2 planes][rows_cap][ffn]
     // LM-head epilogue
     unsigned long long *keys;
     float *logits;
@@ -62,7 +64,8 @@ template <int N>
 struct GemmShape {
     static constexpr int BM = 128, BK = 64;
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = N * BK * 2;
+    static constexpr int B_PLANE = N * BK * 2;      // one of the hi / lo planes
+    static constexpr int B_BYTES = 2 * B_PLANE;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES_RAW = (104 * 1024) / STAGE_BYTES;  // two CTAs per SM
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
@@ -70,7 +73,7 @@ struct GemmShape {
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
     static constexpr uint32_t IDESC = idesc_bf16(128, N);
     static_assert(STAGES >= 2, "pipeline too shallow");
-    static_assert(B_BYTES % 1024 == 0, "B stage must keep 1024-byte alignment");
+    static_assert(B_PLANE % 1024 == 0, "B planes must keep 1024-byte alignment");
 };
 
 constexpr int kGemmThreads = 192;
@@ -136,7 +139,10 @@ __device__ __forceinline__ void epi_qkv_row(const GemmArgs &a, float rstd, int t
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int fs = fbase + lane + 32 * i;
-            a.q_out[(static_cast<size_t>(r) * a.nq + fs / D) * D + fs % D] = __float2bfloat16(x[i]);
+            const size_t o = (static_cast<size_t>(r) * a.nq + fs / D) * D + fs % D;
+            const Bf16Pair pr = split_bf16(x[i]);
+            a.q_out[o] = pr.hi;
+            a.q_out[o + static_cast<size_t>(a.rows_cap) * a.nq * D] = pr.lo;
         }
         return;
     }
@@ -167,7 +173,9 @@ __device__ __forceinline__ void epi_resid_row(const GemmArgs &a, int tile, int r
             const size_t o = static_cast<size_t>(r) * a.hidden + F;
             const float xn = a.x[o] + x[i];
             a.x[o] = xn;
-            a.xb[o] = __float2bfloat16(xn * __bfloat162float(a.g_next[F]));
+            const Bf16Pair pr = split_bf16(xn * __bfloat162float(a.g_next[F]));
+            a.xb[o] = pr.hi;
+            a.xb[o + static_cast<size_t>(a.rows_cap) * a.hidden] = pr.lo;
             sq += xn * xn;
         }
     }
@@ -183,7 +191,10 @@ __device__ __forceinline__ void epi_swiglu_row(const GemmArgs &a, float rstd, in
         const int F = tile * 64 + lane + 32 * i;
         if (F < a.n_out) {
             const float gt = x[i] * rstd, up = x[i + 2] * rstd;
-            a.h_out[static_cast<size_t>(r) * a.n_out + F] = __float2bfloat16(gt / (1.f + __expf(-gt)) * up);
+            const size_t o = static_cast<size_t>(r) * a.n_out + F;
+            const Bf16Pair pr = split_bf16(gt / (1.f + __expf(-gt)) * up);
+            a.h_out[o] = pr.hi;
+            a.h_out[o + static_cast<size_t>(a.rows_cap) * a.n_out] = pr.lo;
         }
     }
 }
@@ -321,7 +332,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             for (int i = pre; i < ahead; ++i) prefetch_a<KIND>(&tmA0, &tmA1, &tmA2, a, tile, (kb0 + i) * 64);
             pdl_wait();  // activations come from the previous kernel
             for (int i = 0; i < pre; ++i)
-                tma_load_2d(smem + i * S::STAGE_BYTES + S::A_BYTES, &tmB, &full_bar[i], (kb0 + i) * 64, 0);
+                tma_load_3d(smem + i * S::STAGE_BYTES + S::A_BYTES, &tmB, &full_bar[i], (kb0 + i) * 64, 0, 0);
             for (int i = pre; i < nk; ++i) {
                 const int s = i % S::STAGES;
                 const uint32_t ph = (i / S::STAGES) & 1;
@@ -333,7 +344,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 uint8_t *sa = smem + s * S::STAGE_BYTES;
                 const int kc = (kb0 + i) * 64;
                 load_a<KIND>(sa, &tmA0, &tmA1, &tmA2, &full_bar[s], a, tile, kc, pol_w);
-                tma_load_2d(sa + S::A_BYTES, &tmB, &full_bar[s], kc, 0);
+                tma_load_3d(sa + S::A_BYTES, &tmB, &full_bar[s], kc, 0, 0);
             }
         }
     } else if (warp == 5) {
@@ -347,10 +358,13 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 }
                 tc_fence_after();
                 const uint64_t ad = sw128_desc(smem_u32(smem + s * S::STAGE_BYTES));
-                const uint64_t bd = sw128_desc(smem_u32(smem + s * S::STAGE_BYTES + S::A_BYTES));
+                const uint64_t bh = sw128_desc(smem_u32(smem + s * S::STAGE_BYTES + S::A_BYTES));
+                const uint64_t bl = sw128_desc(smem_u32(smem + s * S::STAGE_BYTES + S::A_BYTES + S::B_PLANE));
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    umma_bf16(tmem, ad + 2 * k, bd + 2 * k, S::IDESC, (i > 0 || k > 0) ? 1u : 0u);
+                for (int k = 0; k < 4; ++k) {
+                    umma_bf16(tmem, ad + 2 * k, bh + 2 * k, S::IDESC, (i > 0 || k > 0) ? 1u : 0u);
+                    umma_bf16(tmem, ad + 2 * k, bl + 2 * k, S::IDESC, 1u);
+                }
                 umma_commit(&empty_bar[s]);
             }
             umma_commit(&accum_bar);

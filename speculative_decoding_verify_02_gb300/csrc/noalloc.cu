@@ -149,7 +149,7 @@ extern "C" int sdv_paged_attention_noalloc(const void *d_q, const void *d_kv_lay
     const int grp = n_q_heads / n_kv_heads;
     if (grp > 8 || 128 % grp) return SDV_ERR_UNSUPPORTED;
     // rows of one work item: grp heads x the span rows handled per launch
-    const int qrows = std::min(max_span, 128 / grp);
+    const int qrows = std::min(max_span, kAttnRows / grp);
     const int max_work = B * ((max_context + kAttnGroup - 1) / kAttnGroup);
     const Layout L = layout(B, n_kv_heads, head_dim, grp * qrows, max_work);
     if (L.total > kScratchBytes) return SDV_ERR_CAPACITY;  // past the 8 MiB scratch: use sdv_op_attention
@@ -171,13 +171,13 @@ extern "C" int sdv_paged_attention_noalloc(const void *d_q, const void *d_kv_lay
 
     AttnArgs a{};
     a.q = static_cast<const bf16 *>(d_q);
+    a.q_plane = 0;
+    a.out_plane = 0;
     a.kv_layer = static_cast<const bf16 *>(d_kv_layer);
     a.page_table = d_page_table;
     a.pages_per_seq = pages_per_seq;
     a.page_size = page_size;
     a.n_pages = n_pages;
-    a.seq_base = d_base;
-    a.row_off = d_row_off;
     a.work = work;
     a.n_work = n_work;
     a.nq = n_q_heads;

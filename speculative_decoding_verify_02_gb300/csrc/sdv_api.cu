@@ -148,7 +148,7 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     const int qdim = m.n_q_heads * D, kvdim = m.n_kv_heads * D;
     const int pps = ceil_div(c.max_context, c.page_size);
     const int grp = m.n_q_heads / m.n_kv_heads;
-    const int qrows = 128 / grp;
+    const int qrows = kAttnRows / grp;
     const int work_cap = ceil_div(static_cast<long long>(c.n_pages) * c.page_size, kAttnGroup) + B;
     const int ng_slots = c.ngram_capacity > 0 ? next_pow2(std::max(16, 2 * c.ngram_capacity)) : 0;
     const int ss_tiles = ceil_div(H, 128);
@@ -193,11 +193,11 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     s.ng_slots = ng_slots;
 
     float *x = reinterpret_cast<float *>(take(sizeof(float) * kRowsCap * H));
-    bf16 *xb = reinterpret_cast<bf16 *>(take(sizeof(bf16) * kRowsCap * H));
+    bf16 *xb = reinterpret_cast<bf16 *>(take(sizeof(bf16) * 2 * kRowsCap * H));        // hi, lo planes
     float *ss = reinterpret_cast<float *>(take(sizeof(float) * ss_tiles * kRowsCap));
-    bf16 *q = reinterpret_cast<bf16 *>(take(sizeof(bf16) * kRowsCap * qdim));
-    bf16 *ao = reinterpret_cast<bf16 *>(take(sizeof(bf16) * kRowsCap * qdim));
-    bf16 *hb = reinterpret_cast<bf16 *>(take(sizeof(bf16) * kRowsCap * F));
+    bf16 *q = reinterpret_cast<bf16 *>(take(sizeof(bf16) * 2 * kRowsCap * qdim));
+    bf16 *ao = reinterpret_cast<bf16 *>(take(sizeof(bf16) * 2 * kRowsCap * qdim));
+    bf16 *hb = reinterpret_cast<bf16 *>(take(sizeof(bf16) * 2 * kRowsCap * F));
     float *part[5];
     int *cnt[5];
     for (int i = 0; i < 5; ++i) {
@@ -271,6 +271,20 @@ EncodeTiledFn get_encoder() {
             fn = reinterpret_cast<EncodeTiledFn>(p);
     }
     return fn;
+}
+
+// 3-D bf16 map over the hi/lo planes of an activation buffer [2][rows][cols]; box = 64 columns x
+// box_rows rows x both planes, 128-byte swizzle (the planes land one after the other in shared memory).
+bool encode_planes(CUtensorMap *tm, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    EncodeTiledFn enc = get_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {cols, rows, 2};
+    cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+    cuuint32_t box[3] = {64, box_rows, 2};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D bf16 map over a row-major [rows][cols] matrix; box = 64 columns x box_rows rows, 128-byte swizzle.
@@ -419,18 +433,18 @@ GemmArgs base_args(const sdv_ctx *ctx, int kind, int pidx) {
 }
 
 // Paged attention of `layer` over the rows prepared in the device state.
-int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, bf16 *out, int max_rows, int max_span, cudaStream_t st) {
-    (void)max_rows;
+int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *out, size_t out_plane, int max_span,
+                  cudaStream_t st) {
     const sdv_model_cfg &m = ctx->m;
     AttnArgs a{};
     a.q = q;
+    a.q_plane = q_plane;
+    a.out_plane = out_plane;
     a.kv_layer = ctx->pool + ctx->layer_stride * layer;
     a.page_table = ctx->st.page_table;
     a.pages_per_seq = ctx->pages_per_seq;
     a.page_size = ctx->c.page_size;
     a.n_pages = ctx->c.n_pages;
-    a.seq_base = ctx->st.seq_base;
-    a.row_off = ctx->st.row_off;
     a.work = ctx->st.work;
     a.n_work = ctx->st.n_work;
     a.nq = m.n_q_heads;
@@ -569,9 +583,9 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
     }
     ok &= encode_2d(&ctx->tm_lm, w->lm_head, m->vocab, H, 128);
     for (int i = 0; i < 4 && ok; ++i) {
-        ok &= encode_2d(&ctx->tm_xb[i], ctx->xb, kRowsCap, H, kNs[i]);
-        ok &= encode_2d(&ctx->tm_ao[i], ctx->attn_o, kRowsCap, qdim, kNs[i]);
-        ok &= encode_2d(&ctx->tm_h[i], ctx->h, kRowsCap, F, kNs[i]);
+        ok &= encode_planes(&ctx->tm_xb[i], ctx->xb, kRowsCap, H, kNs[i]);
+        ok &= encode_planes(&ctx->tm_ao[i], ctx->attn_o, kRowsCap, qdim, kNs[i]);
+        ok &= encode_planes(&ctx->tm_h[i], ctx->h, kRowsCap, F, kNs[i]);
     }
     if (!ok) {
         delete ctx;
@@ -675,7 +689,8 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
         if (e != cudaSuccess) return SDV_ERR_CUDA;
         {
             PhaseMark pm(ctx, 2, st);
-            r = run_attention(ctx, l, ctx->q, ctx->attn_o, max_rows, max_span, st);
+            const size_t plane = static_cast<size_t>(kRowsCap) * m.n_q_heads * m.head_dim;
+            r = run_attention(ctx, l, ctx->q, plane, ctx->attn_o, plane, max_span, st);
         }
         if (r) return r;
         // O projection + residual; emits bf16(x * g_ffn) and sum-of-squares parts. Its weights
@@ -872,8 +887,7 @@ int sdv_op_attention(sdv_ctx *ctx, int layer, const void *d_q, const int32_t *d_
     const int max_rows = ctx->c.max_rows;
     int r = prepare(ctx, nullptr, d_row_off, d_base, B, max_rows, max_span, 0, st);
     if (r) return r;
-    return run_attention(ctx, layer, static_cast<const bf16 *>(d_q), static_cast<bf16 *>(d_out), max_rows, max_span,
-                         st);
+    return run_attention(ctx, layer, static_cast<const bf16 *>(d_q), 0, static_cast<bf16 *>(d_out), 0, max_span, st);
 }
 
 }  // extern "C"

@@ -75,7 +75,7 @@ struct PrepArgs {
     const bf16 *E;       // [vocab][H]
     const bf16 *g0;      // first RMSNorm gain [H]
     float *x;            // [rows_cap][H]
-    bf16 *xb;            // [rows_cap][H]
+    bf16 *xb;            // [2 planes: hi, lo][rows_cap][H]
     float *ss;           // [ss_tiles][rows_cap]
     unsigned long long *keys;  // [rows_cap]
     int H, vocab, rows_cap;
@@ -176,7 +176,9 @@ __global__ void prepare_kernel(PrepArgs p) {
         const int f = t * 128 + threadIdx.x;
         if (t < ntile && f < p.H) {
             p.x[static_cast<size_t>(r) * p.H + f] = vals[t];
-            p.xb[static_cast<size_t>(r) * p.H + f] = __float2bfloat16(vals[t] * __bfloat162float(p.g0[f]));
+            const Bf16Pair pr = split_bf16(vals[t] * __bfloat162float(p.g0[f]));
+            p.xb[static_cast<size_t>(r) * p.H + f] = pr.hi;
+            p.xb[(static_cast<size_t>(p.rows_cap) + r) * p.H + f] = pr.lo;
         }
         if (t < ntile) {
             const float sq = warp_sum(vals[t] * vals[t]);

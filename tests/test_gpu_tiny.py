@@ -45,7 +45,7 @@ def test_tiny_prefill_logits(tiny):
     host, dev, model = tiny
     v = _verifier(dev)
     prompt = workloads.motif_prompt(1)
-    ref = model.forward([oracle.SeqCache(synth.TINY, 256)], [prompt])[0]
+    ref = model.forward([oracle.SeqCache(synth.TINY, 256, kv_dtype="bf16")], [prompt])[0]
     v.ensure_capacity(_t([128]), 1)
     am = _t(np.zeros(128))
     lg = torch.zeros(128, synth.TINY.vocab, dtype=torch.float32, device="cuda")
@@ -60,7 +60,8 @@ def test_tiny_spec_loop_teacher_forced(tiny):
     import torch
     host, dev, model = tiny
     prompt = workloads.motif_prompt(1)
-    streams, recs, pool = oracle.generate(model, [prompt], 32, drafter="ngram", k=4, keep_logits=True)
+    streams, recs, pool = oracle.generate(model, [prompt], 32, drafter="ngram", k=4, keep_logits=True,
+                                          kv_dtype="bf16")
     v = _verifier(dev)
     # prefill in one chunk, as the oracle does (prefill_chunk 128)
     v.ensure_capacity(_t([128]), 1)
