@@ -1,4 +1,4 @@
-"""Writes tests/golden/tiny_config1_oracle.txt from the oracle alone.
+"""Writes tests/golden/tiny_ngram_k4_oracle.txt from the oracle alone.
 
 Run from the repository root:  python tests/golden/make_golden.py
 The file records the oracle's greedy spec loop on the tiny decoder (seed 1,
@@ -23,7 +23,7 @@ def main():
     model = oracle.DenseDecoder(synth.TINY, lambda n: W[n])
     streams, recs, _ = oracle.generate(model, [workloads.motif_prompt(1)], 32, drafter="ngram", k=4,
                                        keep_logits=True)
-    out = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tiny_config1_oracle.txt")
+    out = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tiny_ngram_k4_oracle.txt")
     with open(out, "w") as f:
         f.write("# Oracle output, tiny decoder (seed 1), 128-token motif prompt, 2-gram lookup, K=4, 32 tokens.\n")
         f.write("# Written by tests/golden/make_golden.py (oracle only).\n")

@@ -50,7 +50,7 @@ def _forward(v, tokens, row_off, B, max_span, logits=True):
 
 
 def test_verify_step_parity_848_context(model):
-    """Config-2 shape at 848 tokens: prefill, then an S=8 verify with uniform drafts."""
+    """4B shape, batch 1, 848-token context: prefill, then an S=8 verify with uniform drafts."""
     import torch
     from speculative_decoding_verify_02_gb300.runner import SpecLoop
     host, dev, om = model

@@ -150,7 +150,7 @@ def test_graph_replay_ragged_and_truncated_spans_match_eager(tiny):
 
 
 def test_ngram_loop_spec_on_equals_spec_off(tiny):
-    """Config-1 loop on the device (2-gram lookup, K=4, 32 tokens) gives the same
+    """The tiny-model loop on the device (2-gram lookup, K=4, 32 tokens) gives the same
     stream as the device's plain loop, and commits 1..K+1 tokens per step."""
     _, dev, om = tiny
     prompt = workloads.motif_prompt(1)

@@ -206,9 +206,9 @@ def test_truncation_at_output_budget(tiny_model):
     assert len(s[0]) == 9
 
 
-def test_oracle_reproduces_its_recorded_config1_run(tiny_model):
+def test_oracle_reproduces_its_recorded_ngram_k4_run(tiny_model):
     # Regression pin: the stored run was written by tests/golden/make_golden.py (oracle only).
-    rows = list(_rows("tiny_config1_oracle.txt"))
+    rows = list(_rows("tiny_ngram_k4_oracle.txt"))
     stream = _ints(rows[0][1])
     s, rec, _ = generate(tiny_model, [workloads.motif_prompt(1)], 32, drafter="ngram", k=4)
     assert s[0] == stream
