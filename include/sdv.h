@@ -231,12 +231,28 @@ int sdv_op_attention(sdv_ctx *ctx, int layer, const void *d_q, const int32_t *d_
  * records CUDA events around each launch group on its stream; this removes
  * the launch overlap between kernels, so durations are those of each kernel
  * run on its own. Groups: 0 prepare/embed, 1 QKV GEMM, 2 attention, 3 O GEMM,
- * 4 gate/up GEMM, 5 down GEMM, 6 LM-head GEMM. */
+ * 4 gate/up GEMM, 5 down GEMM, 6 LM-head GEMM (launch-per-projection path),
+ * 7 the persistent forward (every layer and the LM head in one launch). */
 int sdv_profile_enable(sdv_ctx *ctx, int on);
 
 /* Synchronise, add the elapsed milliseconds and launch counts of every
- * recorded group into h_ms[7] and h_count[7], and clear the record. */
+ * recorded group into h_ms[8] and h_count[8], and clear the record. */
 int sdv_profile_read(sdv_ctx *ctx, float *h_ms, int32_t *h_count);
+
+/* Timeline of the persistent forward. With d_buf non-null, every later
+ * sdv_spec_forward on the persistent path writes, for each CTA c (one per
+ * SM) and phase p (5 per layer: QKV, attention, O, gate/up, down; then the LM
+ * head), eight %globaltimer stamps in nanoseconds at d_buf[(c * phases + p) * 8
+ * + e]: e = 0 the phase's inputs were ready, 1 its last MMA was issued, 2 its
+ * epilogue (or attention) work finished, 3 its last weight load was issued;
+ * attention phases, first item: 4 K/V and Q landed, 5 softmax and P.V done,
+ * 6 partial parked, 7 merge done; GEMM phases, first segment: 4 accumulator
+ * ready, 5 partial parked, 6 partials of a split tile loaded for its
+ * reduction. Entries of events that did not happen keep their old value. The
+ * buffer (uint64, 8-byte aligned, at least sm_count * phases * 64 bytes, else
+ * SDV_ERR_ARG) stays the caller's; d_buf = NULL stops tracing. The pages have
+ * no counterpart of this call: it is instrumentation. */
+int sdv_fwd_trace(sdv_ctx *ctx, void *d_buf, size_t bytes);
 
 /* Paged attention without any device allocation, for callers that cannot
  * call cudaMalloc: code running while a CUDA graph is being captured,

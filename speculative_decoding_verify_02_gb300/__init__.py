@@ -31,8 +31,10 @@ EXPORTS = (
     "sdv_spec_forward", "sdv_accept_greedy", "sdv_rewind_cache", "sdv_cache_seq_len", "sdv_page_table",
     "sdv_ngram_commit", "sdv_gen_init", "sdv_propose", "sdv_reset_seq", "sdv_get_status", "sdv_status_str",
     "sdv_op_attention", "sdv_profile_enable", "sdv_profile_read", "sdv_paged_attention_noalloc",
+    "sdv_fwd_trace",
 )
-PHASES = ("prepare", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm")
+PHASES = ("prepare", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm",
+          "forward")
 
 
 class SdvError(RuntimeError):
@@ -99,6 +101,7 @@ def lib():
     L.sdv_op_attention.argtypes = [vp, i32, vp, vp, vp, i32, i32, vp, vp]
     L.sdv_profile_enable.argtypes = [vp, i32]
     L.sdv_profile_read.argtypes = [vp, P(ctypes.c_float), P(ctypes.c_int32)]
+    L.sdv_fwd_trace.argtypes = [vp, vp, ctypes.c_size_t]
     L.sdv_paged_attention_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
     for name in EXPORTS:
         if name != "sdv_status_str":
@@ -246,10 +249,16 @@ class Verifier:
 
     def profile_read(self):
         """{phase: (total ms, launches)} since the last read (synchronises)."""
-        ms = (ctypes.c_float * 7)()
-        cnt = (ctypes.c_int32 * 7)()
+        ms = (ctypes.c_float * len(PHASES))()
+        cnt = (ctypes.c_int32 * len(PHASES))()
         _check(lib().sdv_profile_read(self.ctx, ms, cnt), "profile_read")
-        return {PHASES[i]: (ms[i], cnt[i]) for i in range(7)}
+        return {PHASES[i]: (ms[i], cnt[i]) for i in range(len(PHASES))}
+
+    def fwd_trace(self, buf):
+        """Record the persistent forward's per-CTA, per-phase timeline into `buf`
+        (a uint64 device tensor of sm_count x phases x 8), or stop with None."""
+        n = buf.numel() * buf.element_size() if buf is not None else 0
+        _check(lib().sdv_fwd_trace(self.ctx, _ptr(buf) if buf is not None else None, n), "fwd_trace")
 
     def op_attention(self, layer, q, row_off, base, B, max_span, out, stream=None):
         _check(lib().sdv_op_attention(self.ctx, layer, _ptr(q), _ptr(row_off), _ptr(base), B, max_span, _ptr(out),

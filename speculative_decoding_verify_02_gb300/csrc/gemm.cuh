@@ -91,7 +91,15 @@ struct EpiSmem {
     int last;
 };
 
-__device__ __forceinline__ void epi_qkv_row(const GemmArgs &a, float rstd, int tile, int r, int lane, float (&x)[4]) {
+// Per-layer arguments of the row epilogues (the rest comes from GemmArgs).
+struct EpiLayer {
+    const bf16 *q_gain, *k_gain;  // QKV: head-norm gains
+    bf16 *kv_layer;               // QKV: this layer's KV pool
+    const bf16 *g_next;           // residual: gain of the RMSNorm that consumes x
+};
+
+__device__ __forceinline__ void epi_qkv_row(const GemmArgs &a, const EpiLayer &el, float rstd, int tile, int r,
+                                            int lane, float (&x)[4]) {
     const int D = a.D;
     int section, fbase;  // 0 = q, 1 = k, 2 = v; first feature of the tile inside its section
     if (tile < a.q_tiles) {
@@ -108,7 +116,7 @@ __device__ __forceinline__ void epi_qkv_row(const GemmArgs &a, float rstd, int t
     for (int i = 0; i < 4; ++i) x[i] *= rstd;
     const int pos = a.row_pos[r];
     if (section < 2) {
-        const bf16 *gain = section == 0 ? a.q_gain : a.k_gain;
+        const bf16 *gain = section == 0 ? el.q_gain : el.k_gain;
         const int p = pos < 0 ? 0 : (pos >= a.rope_rows ? a.rope_rows - 1 : pos);
         if (D == 128) {  // one head: dims l, l+32, l+64, l+96; pairs (l, l+64), (l+32, l+96)
             if (a.qk_norm) {
@@ -160,20 +168,21 @@ __device__ __forceinline__ void epi_qkv_row(const GemmArgs &a, float rstd, int t
         const size_t off =
             (((static_cast<size_t>(page) * 2 + (section - 1)) * a.nkv + fs / D) * a.page_size + pos % a.page_size) * D +
             fs % D;
-        a.kv_layer[off] = __float2bfloat16(x[i]);
+        el.kv_layer[off] = __float2bfloat16(x[i]);
     }
 }
 
-__device__ __forceinline__ void epi_resid_row(const GemmArgs &a, int tile, int r, int lane, float (&x)[4]) {
+__device__ __forceinline__ void epi_resid_row(const GemmArgs &a, const EpiLayer &el, int tile, int r, int lane,
+                                              float (&x)[4]) {
     float sq = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int F = tile * 128 + lane + 32 * i;
         if (F < a.n_out) {
             const size_t o = static_cast<size_t>(r) * a.hidden + F;
-            const float xn = a.x[o] + x[i];
+            const float xn = __ldcg(&a.x[o]) + x[i];
             a.x[o] = xn;
-            const Bf16Pair pr = split_bf16(xn * __bfloat162float(a.g_next[F]));
+            const Bf16Pair pr = split_bf16(xn * __bfloat162float(el.g_next[F]));
             a.xb[o] = pr.hi;
             a.xb[o + static_cast<size_t>(a.rows_cap) * a.hidden] = pr.lo;
             sq += xn * xn;
@@ -222,10 +231,10 @@ __device__ __forceinline__ void epi_lmhead_row(const GemmArgs &a, float rstd, in
 }
 
 template <int KIND>
-__device__ __forceinline__ void epi_row(const GemmArgs &a, const EpiSmem &es, int tile, int r, int lane,
-                                        float (&x)[4]) {
-    if constexpr (KIND == EPI_QKV) epi_qkv_row(a, es.rstd[r], tile, r, lane, x);
-    else if constexpr (KIND == EPI_RESID) epi_resid_row(a, tile, r, lane, x);
+__device__ __forceinline__ void epi_row(const GemmArgs &a, const EpiLayer &el, const EpiSmem &es, int tile, int r,
+                                        int lane, float (&x)[4]) {
+    if constexpr (KIND == EPI_QKV) epi_qkv_row(a, el, es.rstd[r], tile, r, lane, x);
+    else if constexpr (KIND == EPI_RESID) epi_resid_row(a, el, tile, r, lane, x);
     else if constexpr (KIND == EPI_SWIGLU) epi_swiglu_row(a, es.rstd[r], tile, r, lane, x);
     else epi_lmhead_row(a, es.rstd[r], tile, r, lane, x);
 }
@@ -428,7 +437,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) x[i] = red[r * 128 + lane + 32 * i];
             }
-            epi_row<KIND>(a, es, tile, r, lane, x);
+            epi_row<KIND>(a, EpiLayer{a.q_gain, a.k_gain, a.kv_layer, a.g_next}, es, tile, r, lane, x);
         }
     }
     if (clustered) cluster_sync();  // no CTA leaves while its partial may still be read

@@ -4,12 +4,14 @@
 #include <cmath>
 #include <cstdio>
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
 
 #include "attention.cuh"
 #include "common.cuh"
+#include "fwd.cuh"
 #include "gemm.cuh"
 #include "small.cuh"
 
@@ -41,6 +43,41 @@ int next_pow2(int v) {
     int p = 1;
     while (p < v) p <<= 1;
     return p;
+}
+
+// Most CTAs that share one tile of a plan when its (tile, k-block) units are cut evenly over G CTAs.
+// Split-tile holder table of one plan: [tiles + 1] offsets, then for each tile the partial slots
+// (2c for CTA c's first segment, 2c + 1 for its last) of the CTAs holding its units, in CTA order.
+void holder_table(int tiles, int k_blocks, int G, std::vector<int> &out) {
+    const long long U = static_cast<long long>(tiles) * k_blocks;
+    std::vector<int> off(tiles + 1), slots;
+    for (int t = 0; t < tiles; ++t) {
+        off[t] = static_cast<int>(slots.size());
+        for (long long u = static_cast<long long>(t) * k_blocks; u < static_cast<long long>(t + 1) * k_blocks;) {
+            const long long cc = ((u + 1) * G - 1) / U;
+            const long long first_tile = (cc * U / G) / k_blocks;
+            slots.push_back(static_cast<int>(2 * cc + (t == first_tile ? 0 : 1)));
+            u = (cc + 1) * U / G;
+        }
+    }
+    off[tiles] = static_cast<int>(slots.size());
+    out.insert(out.end(), off.begin(), off.end());
+    out.insert(out.end(), slots.begin(), slots.end());
+}
+
+int max_holders(int tiles, int k_blocks, int G) {
+    const long long U = static_cast<long long>(tiles) * k_blocks;
+    int best = 0;
+    for (int t = 0; t < tiles; ++t) {
+        int n = 0;
+        for (long long u = static_cast<long long>(t) * k_blocks; u < static_cast<long long>(t + 1) * k_blocks;) {
+            const long long cc = ((u + 1) * G - 1) / U;
+            ++n;
+            u = (cc + 1) * U / G;
+        }
+        best = std::max(best, n);
+    }
+    return best;
 }
 
 GemmPlan make_plan(int tiles, int k_blocks, int sm_count) {
@@ -78,6 +115,24 @@ struct sdv_ctx {
     float *attn_po = nullptr;
     float2 *attn_pml = nullptr;
     int *attn_cnt = nullptr;
+    // persistent forward
+    bool use_fwd = true, fwd_coop = true;
+    int *fwd_sync = nullptr, *fwd_done = nullptr, *fwd_tile_cnt = nullptr, *fwd_att_cnt = nullptr;
+    int *fwd_abort = nullptr, *fwd_n_items = nullptr;
+    int n_sync = 0, fwd_item_cap = 0, fwd_rps = 0, fwd_max_slices = 0, fwd_tile_stride = 0;
+    int4 *fwd_items = nullptr;
+    float *fwd_part = nullptr, *fwd_att_o = nullptr;
+    float2 *fwd_att_ml = nullptr;
+    CUtensorMap *fwd_tm = nullptr;   // device table: per layer wq wk wv wo wg wu wd, LM head, then B maps [4][3]
+    FwdLayer *fwd_layers = nullptr;  // device table
+    int *fwd_hold = nullptr;         // device table of split-tile holders (FwdParams::hold)
+    int fwd_hold_base[5] = {0, 0, 0, 0, 0};
+    std::vector<int> fwd_hold_host;
+    int fwd_l2_ahead = 16;                    // SDV_L2_AHEAD overrides
+    int fwd_ring = 0;                         // ring stages in use, 0 = all; SDV_RING overrides
+    unsigned long long *fwd_trace = nullptr;  // caller's timeline buffer, or nullptr
+    std::vector<CUtensorMap> fwd_tm_host;
+    std::vector<FwdLayer> fwd_layers_host;
     int ss_tiles = 0, grp = 0, qrows = 0, work_cap = 0, pages_per_seq = 0, ng_slots = 0;
     size_t layer_stride = 0;  // pool elements per layer
     GemmPlan plan[5];         // qkv, o, gate/up, down, lm head
@@ -213,6 +268,30 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     float2 *apml = reinterpret_cast<float2 *>(take(sizeof(float2) * nslots));
     int *acnt = reinterpret_cast<int *>(take(sizeof(int) * static_cast<size_t>(B) * m.n_kv_heads * kAttnCluster));
 
+    // persistent forward: completion counters, split-tile counters, attention counters and the
+    // abort flag in one zeroed range; attention items and partials; split-tile partials; tables
+    const int rps = std::max(1, kFwdRows / grp);
+    const int max_slices = ceil_div(c.max_span, rps);
+    const int fchunk_cap = ceil_div(static_cast<long long>(c.n_pages) * c.page_size, kFwdChunk) + B;
+    const int item_cap = fchunk_cap * max_slices;
+    int tile_stride = 0;
+    for (const GemmPlan &p : plans) tile_stride = std::max(tile_stride, p.tiles);
+    const int n_done = 5 * m.n_layers + 1;
+    const int n_att_cnt = B * max_slices * m.n_kv_heads;
+    const int n_sync = n_done + 5 * tile_stride + n_att_cnt + 1;
+    int *fsync = reinterpret_cast<int *>(take(sizeof(int) * static_cast<size_t>(n_sync)));
+    int4 *fitems = reinterpret_cast<int4 *>(take(sizeof(int4) * static_cast<size_t>(item_cap)));
+    int *fn_items = reinterpret_cast<int *>(take(sizeof(int)));
+    float *fpart = reinterpret_cast<float *>(take(sizeof(float) * 2 * static_cast<size_t>(sm_count) * kRowsCap * 128));
+    const size_t att_slots = static_cast<size_t>(item_cap) * m.n_kv_heads * kFwdRows;
+    float *fatt_o = reinterpret_cast<float *>(take(sizeof(float) * att_slots * D));
+    float2 *fatt_ml = reinterpret_cast<float2 *>(take(sizeof(float2) * att_slots));
+    CUtensorMap *ftm = reinterpret_cast<CUtensorMap *>(take(sizeof(CUtensorMap) * (7 * m.n_layers + 1 + 12)));
+    FwdLayer *flay = reinterpret_cast<FwdLayer *>(take(sizeof(FwdLayer) * m.n_layers));
+    size_t n_hold = 0;
+    for (const GemmPlan &p : plans) n_hold += 2 * static_cast<size_t>(p.tiles) + 1 + sm_count;
+    int *fhold = reinterpret_cast<int *>(take(sizeof(int) * n_hold));
+
     if (ctx) {
         ctx->st = s;
         ctx->x = x;
@@ -232,6 +311,24 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
         ctx->attn_po = apo;
         ctx->attn_pml = apml;
         ctx->attn_cnt = acnt;
+        ctx->fwd_sync = fsync;
+        ctx->n_sync = n_sync;
+        ctx->fwd_done = fsync;
+        ctx->fwd_tile_cnt = fsync + n_done;
+        ctx->fwd_att_cnt = fsync + n_done + 5 * tile_stride;
+        ctx->fwd_abort = fsync + n_done + 5 * tile_stride + n_att_cnt;
+        ctx->fwd_items = fitems;
+        ctx->fwd_n_items = fn_items;
+        ctx->fwd_item_cap = item_cap;
+        ctx->fwd_rps = rps;
+        ctx->fwd_max_slices = max_slices;
+        ctx->fwd_tile_stride = tile_stride;
+        ctx->fwd_part = fpart;
+        ctx->fwd_att_o = fatt_o;
+        ctx->fwd_att_ml = fatt_ml;
+        ctx->fwd_tm = ftm;
+        ctx->fwd_layers = flay;
+        ctx->fwd_hold = fhold;
         ctx->ss_tiles = ss_tiles;
         ctx->grp = grp;
         ctx->qrows = qrows;
@@ -494,7 +591,126 @@ int prepare(sdv_ctx *ctx, const int32_t *tokens, const int32_t *row_off, const i
     p.H = ctx->m.hidden;
     p.vocab = ctx->m.vocab;
     p.rows_cap = kRowsCap;
+    p.items = ctx->fwd_items;
+    p.n_items = ctx->fwd_n_items;
+    p.item_cap = ctx->fwd_item_cap;
+    p.item_keys = kFwdChunk;
+    p.rps = ctx->fwd_rps;
+    p.zero = ctx->fwd_sync;
+    p.n_zero = ctx->n_sync;
     return rc(launch(ctx, prepare_kernel, dim3(embed ? 1 + max_rows : 1), dim3(128), 0, st, p));
+}
+
+// Epilogue arguments of the projections, without the per-layer fields.
+GemmArgs qkv_args(const sdv_ctx *ctx) {
+    const sdv_model_cfg &m = ctx->m;
+    GemmArgs a = base_args(ctx, EPI_QKV, P_QKV);
+    a.n_out = (m.n_q_heads + 2 * m.n_kv_heads) * m.head_dim;
+    a.nq = m.n_q_heads;
+    a.nkv = m.n_kv_heads;
+    a.D = m.head_dim;
+    a.q_tiles = m.n_q_heads * m.head_dim / 128;
+    a.k_tiles = m.n_kv_heads * m.head_dim / 128;
+    a.qk_norm = m.qk_norm;
+    a.rope = ctx->rope;
+    a.rope_rows = ctx->c.max_context;
+    a.row_seq = ctx->st.row_seq;
+    a.row_pos = ctx->st.row_pos;
+    a.page_table = ctx->st.page_table;
+    a.pages_per_seq = ctx->pages_per_seq;
+    a.page_size = ctx->c.page_size;
+    a.n_pages = ctx->c.n_pages;
+    a.q_out = ctx->q;
+    return a;
+}
+
+template <int N, int D>
+cudaError_t launch_fwd_nd(const sdv_ctx *ctx, const FwdParams &P, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P.grid);
+    cfg.blockDim = dim3(kFwdThreads);
+    cfg.dynamicSmemBytes = FwdShape<N, D>::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = ctx->fwd_coop ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, fwd_kernel<N, D>, P);
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const sdv_ctx *ctx, int nidx, const FwdParams &P, cudaStream_t st) {
+    switch (nidx) {
+        case 0: return launch_fwd_nd<16, D>(ctx, P, st);
+        case 1: return launch_fwd_nd<32, D>(ctx, P, st);
+        case 2: return launch_fwd_nd<64, D>(ctx, P, st);
+        default: return launch_fwd_nd<128, D>(ctx, P, st);
+    }
+}
+
+// Every layer and the LM head in one persistent launch (fwd.cuh).
+int launch_fwd(sdv_ctx *ctx, int nidx, int32_t *d_argmax, float *d_logits, cudaStream_t st) {
+    const sdv_model_cfg &m = ctx->m;
+    FwdParams P{};
+    P.tm_w = ctx->fwd_tm;
+    P.tm_b = ctx->fwd_tm + 7 * m.n_layers + 1 + 3 * nidx;
+    P.layers = ctx->fwd_layers;
+    P.n_layers = m.n_layers;
+    P.grid = ctx->sm_count;
+    for (int i = 0; i < 5; ++i) P.g[i] = FwdGemm{ctx->plan[i].tiles, ctx->plan[i].k_blocks};
+    P.ga[EPI_QKV] = qkv_args(ctx);
+    GemmArgs r = base_args(ctx, EPI_RESID, P_O);
+    r.n_out = m.hidden;
+    r.x = ctx->x;
+    r.xb = ctx->xb;
+    r.ss_out = ctx->ss;
+    P.ga[EPI_RESID] = r;
+    GemmArgs g = base_args(ctx, EPI_SWIGLU, P_GU);
+    g.n_out = m.ffn;
+    g.h_out = ctx->h;
+    P.ga[EPI_SWIGLU] = g;
+    GemmArgs lm = base_args(ctx, EPI_LMHEAD, P_LM);
+    lm.keys = ctx->keys;
+    lm.logits = d_logits;
+    lm.argmax_out = d_argmax;
+    lm.vocab = m.vocab;
+    P.ga[EPI_LMHEAD] = lm;
+    P.layer_stride = ctx->layer_stride;
+    P.pool = ctx->pool;
+    P.attn_out = ctx->attn_o;
+    P.q_plane = static_cast<size_t>(kRowsCap) * m.n_q_heads * m.head_dim;
+    P.items = ctx->fwd_items;
+    P.n_items = ctx->fwd_n_items;
+    P.row_off = ctx->st.row_off;
+    P.rps = ctx->fwd_rps;
+    P.page_shift = __builtin_ctz(static_cast<unsigned>(ctx->c.page_size));
+    P.max_slices = ctx->fwd_max_slices;
+    P.scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(m.head_dim));
+    P.att_o = ctx->fwd_att_o;
+    P.att_ml = ctx->fwd_att_ml;
+    P.att_cnt = ctx->fwd_att_cnt;
+    P.done = ctx->fwd_done;
+    P.tile_cnt = ctx->fwd_tile_cnt;
+    P.tile_stride = ctx->fwd_tile_stride;
+    P.part = ctx->fwd_part;
+    P.abort_flag = ctx->fwd_abort;
+    P.trace = ctx->fwd_trace;
+    P.l2_ahead = ctx->fwd_l2_ahead;
+    P.hold = ctx->fwd_hold;
+    for (int i = 0; i < 5; ++i) P.hold_base[i] = ctx->fwd_hold_base[i];
+    P.ring = ctx->fwd_ring;
+    const cudaError_t e = m.head_dim == 128 ? launch_fwd_d<128>(ctx, nidx, P, st) : launch_fwd_d<64>(ctx, nidx, P, st);
+    return rc(e);
+}
+
+template <int D>
+cudaError_t set_fwd_smem_d() {
+    cudaError_t e = set_smem(fwd_kernel<16, D>, FwdShape<16, D>::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(fwd_kernel<32, D>, FwdShape<32, D>::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(fwd_kernel<64, D>, FwdShape<64, D>::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(fwd_kernel<128, D>, FwdShape<128, D>::SMEM_BYTES);
+    return e;
 }
 
 }  // namespace
@@ -599,9 +815,70 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
     if (e == cudaSuccess) e = set_gemm_smem<128>();
     if (e == cudaSuccess) e = set_smem(attn_kernel<128>, AttnShape<128>::SMEM);
     if (e == cudaSuccess) e = set_smem(attn_kernel<64>, AttnShape<64>::SMEM);
+    if (e == cudaSuccess) e = D == 128 ? set_fwd_smem_d<128>() : set_fwd_smem_d<64>();
     if (e != cudaSuccess) {
         delete ctx;
         return SDV_ERR_CUDA;
+    }
+
+    // The persistent forward needs one co-resident CTA per SM.
+    {
+        int coop = 0, occ = 0;
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+        cudaError_t oe = D == 128 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fwd_kernel<128, 128>, kFwdThreads,
+                                                                                  FwdShape<128, 128>::SMEM_BYTES)
+                                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fwd_kernel<128, 64>, kFwdThreads,
+                                                                                  FwdShape<128, 64>::SMEM_BYTES);
+        if (oe != cudaSuccess) cudaGetLastError();
+        ctx->fwd_coop = coop != 0;
+        ctx->use_fwd = oe == cudaSuccess && occ >= 1;
+        // SDV_FORWARD=persistent selects the persistent forward; the default is one launch per projection
+        const char *ev = std::getenv("SDV_FORWARD");
+        if (!(ev && std::strcmp(ev, "persistent") == 0)) ctx->use_fwd = false;
+        if (c->page_size & (c->page_size - 1)) ctx->use_fwd = false;  // page index by shift
+        const char *la = std::getenv("SDV_L2_AHEAD");
+        if (la) ctx->fwd_l2_ahead = std::max(0, std::atoi(la));
+        const char *rg = std::getenv("SDV_RING");
+        if (rg) ctx->fwd_ring = std::max(0, std::atoi(rg));
+        // the kernel's unit arithmetic is 32-bit, and a split tile's partials must fit its staging region
+        const int att = D == 128 ? FwdShape<16, 128>::ATT : FwdShape<16, 64>::ATT;
+        for (int i = 0; i < 5; ++i) {
+            const long long U = static_cast<long long>(ctx->plan[i].tiles) * ctx->plan[i].k_blocks;
+            if (U * (sms + 1) >= (1ll << 31)) ctx->use_fwd = false;
+            const int mh = max_holders(ctx->plan[i].tiles, ctx->plan[i].k_blocks, sms);
+            if (mh > kFwdMaxHolders || mh * 512 > att) ctx->use_fwd = false;
+        }
+    }
+    ctx->fwd_tm_host.resize(7 * m->n_layers + 1 + 12);
+    for (int l = 0; l < m->n_layers; ++l) {
+        CUtensorMap *t = &ctx->fwd_tm_host[7 * l];
+        t[0] = ctx->tm_wq[l];
+        t[1] = ctx->tm_wk[l];
+        t[2] = ctx->tm_wv[l];
+        t[3] = ctx->tm_wo[l];
+        t[4] = ctx->tm_wg[l];
+        t[5] = ctx->tm_wu[l];
+        t[6] = ctx->tm_wd[l];
+    }
+    ctx->fwd_tm_host[7 * m->n_layers] = ctx->tm_lm;
+    for (int i = 0; i < 4; ++i) {
+        CUtensorMap *t = &ctx->fwd_tm_host[7 * m->n_layers + 1 + 3 * i];
+        t[0] = ctx->tm_xb[i];
+        t[1] = ctx->tm_ao[i];
+        t[2] = ctx->tm_h[i];
+    }
+    ctx->fwd_hold_host.clear();
+    for (int i = 0; i < 5; ++i) {
+        ctx->fwd_hold_base[i] = static_cast<int>(ctx->fwd_hold_host.size());
+        holder_table(ctx->plan[i].tiles, ctx->plan[i].k_blocks, sms, ctx->fwd_hold_host);
+    }
+    ctx->fwd_layers_host.resize(m->n_layers);
+    for (int l = 0; l < m->n_layers; ++l) {
+        FwdLayer &f = ctx->fwd_layers_host[l];
+        f.q_gain = static_cast<const bf16 *>(ctx->layers[l].q_norm);
+        f.k_gain = static_cast<const bf16 *>(ctx->layers[l].k_norm);
+        f.ffn_norm = static_cast<const bf16 *>(ctx->layers[l].ffn_norm);
+        f.next_norm = static_cast<const bf16 *>(l + 1 < m->n_layers ? ctx->layers[l + 1].attn_norm : w->final_norm);
     }
 
     // RoPE table: cos/sin of pos * theta^(-2j/D), in double on the host.
@@ -618,6 +895,15 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
     e = cudaMemsetAsync(ctx->ws, 0, ws_bytes, st);
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(ctx->rope, ctx->rope_host.data(), ctx->rope_host.size() * sizeof(float2),
+                            cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ctx->fwd_tm, ctx->fwd_tm_host.data(), ctx->fwd_tm_host.size() * sizeof(CUtensorMap),
+                            cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ctx->fwd_layers, ctx->fwd_layers_host.data(), ctx->fwd_layers_host.size() * sizeof(FwdLayer),
+                            cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ctx->fwd_hold, ctx->fwd_hold_host.data(), ctx->fwd_hold_host.size() * sizeof(int),
                             cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) {
         init_state_kernel<<<64, 256, 0, st>>>(ctx->st);
@@ -657,6 +943,10 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
         r = prepare(ctx, d_tokens, d_row_off, nullptr, B, max_rows, max_span, 1, st);
     }
     if (r) return r;
+    if (ctx->use_fwd) {
+        PhaseMark pm(ctx, 7, st);
+        return launch_fwd(ctx, ni, d_argmax, d_logits, st);
+    }
     for (int l = 0; l < m.n_layers; ++l) {
         const sdv_layer_weights &L = ctx->layers[l];
         // QKV projection + q/k head norm + RoPE + paged K/V write
@@ -869,13 +1159,25 @@ int sdv_profile_read(sdv_ctx *ctx, float *h_ms, int32_t *h_count) {
         float ms = 0.f;
         if (cudaEventElapsedTime(&ms, ctx->ev_pool[mk.second.first], ctx->ev_pool[mk.second.second]) != cudaSuccess)
             return SDV_ERR_CUDA;
-        if (mk.first >= 0 && mk.first < 7) {
+        if (mk.first >= 0 && mk.first < 8) {
             h_ms[mk.first] += ms;
             h_count[mk.first] += 1;
         }
     }
     ctx->ev_marks.clear();
     ctx->ev_used = 0;
+    return SDV_OK;
+}
+
+int sdv_fwd_trace(sdv_ctx *ctx, void *d_buf, size_t bytes) {
+    if (!ctx) return SDV_ERR_ARG;
+    if (!d_buf) {
+        ctx->fwd_trace = nullptr;
+        return SDV_OK;
+    }
+    const size_t need = static_cast<size_t>(ctx->sm_count) * (5 * ctx->m.n_layers + 1) * 16 * sizeof(unsigned long long);
+    if (bytes < need || reinterpret_cast<uintptr_t>(d_buf) % 8) return SDV_ERR_ARG;
+    ctx->fwd_trace = static_cast<unsigned long long *>(d_buf);
     return SDV_OK;
 }
 
