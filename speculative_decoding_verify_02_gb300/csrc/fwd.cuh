@@ -27,9 +27,10 @@
 // abort flag that every other wait also watches, waits for its own copies in
 // flight, frees its TMEM and returns.
 //
-// Warp roles (224 threads): warps 0-3 epilogue and attention, warp 4 weight
-// TMA producer, warp 5 tcgen05 MMA issuer (and TMEM owner), warp 6 activation
-// TMA producer.
+// Warp roles (384 threads): warps 0-7 epilogue and attention (warps 0-3, one
+// per TMEM lane quarter, read the accumulators), warp 8 weight TMA producer,
+// warp 9 tcgen05 MMA issuer (and TMEM owner), warp 10 activation TMA producer,
+// warp 11 copier (weight tiles, shared -> tensor memory).
 #pragma once
 
 #include "attention.cuh"
@@ -38,7 +39,11 @@
 
 namespace sdv {
 
-constexpr int kFwdThreads = 224;
+constexpr int kEpiWarps = 8;                        // epilogue and attention warps (0-7)
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kWarpProducerA = kEpiWarps, kWarpMma = kEpiWarps + 1, kWarpProducerB = kEpiWarps + 2;
+constexpr int kWarpCopier = kEpiWarps + 3;
+constexpr int kFwdThreads = kEpiThreads + 128;
 constexpr int kFwdRows = 32;     // attention query rows (heads x span rows) per item
 constexpr int kFwdChunk = 128;   // keys per attention item
 constexpr int kFwdSmemLimit = 232448;
@@ -83,12 +88,11 @@ struct FwdParams {
     int tile_stride;
     float *part;              // [2 * grid][rows_cap][128]
     int *abort_flag;
-    int l2_ahead;             // weight k-blocks the producer prefetches into L2 ahead of its loads
     // split tiles: per plan, at hold + hold_base[i]: [tiles + 1] offsets, then the partial slots of
     // each tile's holders in CTA order (a tile with one holder is not split)
     const int *hold;
     int hold_base[5];
-    int ring;                 // ring stages in use (1..the kernel's shared-memory stages)
+    int ring;                 // weight-ring slots in use (3..the kernel's slots; other values: all)
     // optional timeline: [grid][phases][16] %globaltimer stamps, nullptr when not tracing:
     // 0 inputs ready, 1 last MMA issued, 2 epilogue (or attention) work done, 3 last weight load
     // issued; GEMM epilogue, first segment: 4 accumulator ready, 5 partial parked, 6 split tile's
@@ -239,50 +243,6 @@ __device__ __forceinline__ bool next_holder(int t, int &cc, const FwdGemm &g, in
     return true;
 }
 
-// Walks this CTA's k-blocks of every GEMM phase in the order the ring consumes them.
-struct KCursor {
-    int p, n_ph, nL, c, G, u, u1, KB;
-    __device__ __forceinline__ KCursor(const FwdParams &P, int c_, int G_) {
-        p = 0;
-        nL = P.n_layers;
-        n_ph = 5 * nL + 1;
-        c = c_;
-        G = G_;
-        seek(P);
-    }
-    // from phase p on, the first GEMM phase where this CTA holds units
-    __device__ __forceinline__ void seek(const FwdParams &P) {
-        for (; p < n_ph; ++p) {
-            const int kind = fwd_kind(p, nL);
-            if (kind == FP_ATTN) continue;
-            const FwdGemm &g = P.g[fwd_gemm_index(kind)];
-            const int U = g.tiles * g.kblocks;
-            u = unit_begin(c, U, G);
-            u1 = unit_begin(c + 1, U, G);
-            KB = g.kblocks;
-            if (u < u1) return;
-        }
-    }
-    __device__ __forceinline__ bool valid() const { return p < n_ph; }
-    __device__ __forceinline__ void advance(const FwdParams &P) {
-        if (++u >= u1) {
-            ++p;
-            seek(P);
-        }
-    }
-    __device__ __forceinline__ int kind() const { return fwd_kind(p, nL); }
-    __device__ __forceinline__ int tile() const { return u / KB; }
-    __device__ __forceinline__ int kc() const { return (u % KB) * 64; }
-};
-
-__device__ __forceinline__ void fwd_prefetch_a(int ek, const CUtensorMap *tw, const GemmArgs &a, int t, int kc) {
-    switch (ek) {
-        case EPI_QKV: prefetch_a<EPI_QKV>(tw, tw + 1, tw + 2, a, t, kc); break;
-        case EPI_SWIGLU: prefetch_a<EPI_SWIGLU>(tw, tw + 1, tw, a, t, kc); break;
-        default: prefetch_a<EPI_RESID>(tw, tw, tw, a, t, kc); break;
-    }
-}
-
 // Partial slot of CTA c's segment of tile t: 2c for the CTA's first segment, 2c + 1 for its last.
 __device__ __forceinline__ int part_slot(int t, int c, const FwdGemm &g, int G) {
     const int U = g.tiles * g.kblocks;
@@ -291,6 +251,23 @@ __device__ __forceinline__ int part_slot(int t, int c, const FwdGemm &g, int G) 
 
 
 // ------------------------------------------------------------------ attention items
+constexpr int kRegChunks = 8;  // row slices of at most this many chunks merge in registers
+
+// four output columns num / den as hi and lo bf16 planes (8-byte stores)
+__device__ __forceinline__ void store_out4(bf16 *out, size_t plane, size_t oi, float4 num, float den) {
+    const Bf16Pair p0 = split_bf16(num.x / den), p1 = split_bf16(num.y / den);
+    const Bf16Pair p2 = split_bf16(num.z / den), p3 = split_bf16(num.w / den);
+    __nv_bfloat162 hi01, hi23, lo01, lo23;
+    hi01.x = p0.hi; hi01.y = p1.hi; hi23.x = p2.hi; hi23.y = p3.hi;
+    lo01.x = p0.lo; lo01.y = p1.lo; lo23.x = p2.lo; lo23.y = p3.lo;
+    uint2 hv, lv;
+    hv.x = *reinterpret_cast<uint32_t *>(&hi01);
+    hv.y = *reinterpret_cast<uint32_t *>(&hi23);
+    lv.x = *reinterpret_cast<uint32_t *>(&lo01);
+    lv.y = *reinterpret_cast<uint32_t *>(&lo23);
+    *reinterpret_cast<uint2 *>(out + oi) = hv;
+    *reinterpret_cast<uint2 *>(out + oi + plane) = lv;
+}
 template <int D>
 struct FwdAttnSmem {
     static constexpr int ROW = D * 2;
@@ -302,10 +279,11 @@ struct FwdAttnSmem {
     static_assert(2 * KV_BYTES >= 2 * kFwdRows * D * 4, "key-block partials must fit in the K/V region");
 };
 
-// One attention item (sequence b, span-row slice, 128-key chunk, kv head g) on warps 0-3.
+// One attention item (sequence b, span-row slice, 128-key chunk, kv head g) on warps 0-7.
 // Query row j of the slice is span row q0 + j / grp of q-head g * grp + j % grp and
 // attends positions <= L_b + q0 + j / grp. Warp w runs query tile w & 1 against 64-key
-// block w >> 1; the two blocks merge in shared memory, then the chunk either writes the
+// block (w >> 1) & 1 for half (w >> 2) of the head dimension (both halves compute the same
+// scores); the two blocks merge in shared memory, then the chunk either writes the
 // output (a one-chunk row slice) or parks its partial, and the last chunk of the slice
 // to arrive merges every chunk in chunk order.
 template <int D>
@@ -339,7 +317,7 @@ __device__ void fwd_attn_item(const FwdParams &P, int layer, int item, uint8_t *
     float2 *ml_s = reinterpret_cast<float2 *>(sm + S::ML_OFF);
     float2 *ml2_s = ml_s + kFwdRows;
 
-    for (int e = tid; e < 2 * kFwdRows * CH; e += 128) {  // both planes of rows 0..31 (rows >= M zero-filled)
+    for (int e = tid; e < 2 * kFwdRows * CH; e += kEpiThreads) {  // both planes of rows 0..31 (rows >= M zero-filled)
         const int pl = e / (kFwdRows * CH), j = (e / CH) % kFwdRows, c = e % CH;
         const bool valid = j < M;
         const bf16 *src = qa.q_out;
@@ -352,14 +330,14 @@ __device__ void fwd_attn_item(const FwdParams &P, int layer, int item, uint8_t *
     if (tid == 0) fwd_stamp(P, ph, 4);
     const int ps = P.page_shift, pmask = page_size - 1;
     const int pg0 = k0 >> ps, npg = ((k1 - 1) >> ps) - pg0 + 1;
-    for (int i = tid; i < npg; i += 128) {
+    for (int i = tid; i < npg; i += kEpiThreads) {
         const int slot_idx = pg0 + i;
         page_s[i] = slot_idx < qa.pages_per_seq
                         ? qa.page_table[static_cast<size_t>(b) * qa.pages_per_seq + slot_idx]
                         : -1;
     }
-    named_bar_sync(1, 128);
-    for (int e = tid; e < nblk * kAttnKB * CH; e += 128) {
+    named_bar_sync(1, kEpiThreads);
+    for (int e = tid; e < nblk * kAttnKB * CH; e += kEpiThreads) {
         const int key = e / CH, c = e % CH;
         const int u = k0 + key;
         bool valid = u < k1;
@@ -382,18 +360,18 @@ __device__ void fwd_attn_item(const FwdParams &P, int layer, int item, uint8_t *
     cp_async_commit();
     if (tid == 0) fwd_stamp(P, ph, 5);
     cp_async_wait_all();
-    named_bar_sync(1, 128);
+    named_bar_sync(1, kEpiThreads);
     if (tid == 0) fwd_stamp(P, ph, 6);
 
-    const int mt = warp & 1, blk = warp >> 1;
+    const int mt = warp & 1, blk = (warp >> 1) & 1, dh = warp >> 2;
     const bool active = blk < nblk && mt * 16 < M;
     const int gq = lane >> 2, tq = lane & 3;
     const int jr0 = mt * 16 + gq, jr1 = jr0 + 8;
     const int lim0 = L + q0 + jr0 / grp, lim1 = L + q0 + jr1 / grp;
 
-    float o[D / 8][4];
+    float o[D / 16][4];  // this warp's half of the head dimension
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     if (active) {
         float s[8][4];
@@ -460,10 +438,10 @@ __device__ void fwd_attn_item(const FwdParams &P, int layer, int item, uint8_t *
                 pl[2 * hf + 1] = pack2(x2.lo, x3.lo);
             }
 #pragma unroll
-            for (int dn = 0; dn < D / 8; dn += 2) {
+            for (int dn = 0; dn < D / 16; dn += 2) {
                 const int i = lane >> 3;
                 const int key = blk * kAttnKB + kk * 16 + (i & 1) * 8 + (lane & 7);
-                const int c = dn + (i >> 1);
+                const int c = dh * (D / 16) + dn + (i >> 1);
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4_t(sV + swz<D>(key, c), b0, b1, b2, b3);
                 mma_bf16_16816(o[dn], ph, b0, b1);
@@ -479,33 +457,34 @@ __device__ void fwd_attn_item(const FwdParams &P, int layer, int item, uint8_t *
         l0 = rs0;
         l1 = rs1;
     }
-    named_bar_sync(1, 128);  // K/V no longer read: the region now holds the key blocks' partials
+    named_bar_sync(1, kEpiThreads);  // K/V no longer read: the region now holds the key blocks' partials
     if (tid == 0) fwd_stamp(P, ph, 7);
     if (mt * 16 < Mpad) {
         float *dst = blk == 0 ? po_s : po2_s;
         float2 *mld = blk == 0 ? ml_s : ml2_s;
 #pragma unroll
-        for (int dn = 0; dn < D / 8; ++dn) {
-            *reinterpret_cast<float2 *>(&dst[jr0 * D + dn * 8 + tq * 2]) = make_float2(o[dn][0], o[dn][1]);
-            *reinterpret_cast<float2 *>(&dst[jr1 * D + dn * 8 + tq * 2]) = make_float2(o[dn][2], o[dn][3]);
+        for (int dn = 0; dn < D / 16; ++dn) {
+            const int col = (dh * (D / 16) + dn) * 8 + tq * 2;
+            *reinterpret_cast<float2 *>(&dst[jr0 * D + col]) = make_float2(o[dn][0], o[dn][1]);
+            *reinterpret_cast<float2 *>(&dst[jr1 * D + col]) = make_float2(o[dn][2], o[dn][3]);
         }
-        if (tq == 0) {
+        if (tq == 0 && dh == 0) {
             mld[jr0] = make_float2(m0, l0);
             mld[jr1] = make_float2(m1, l1);
         }
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(1, kEpiThreads);
     // the two key blocks of a row merge with weights exp2(m_block - max); computed once per row,
     // the merged (m, l) replaces block 0's and the weights replace block 1's
-    for (int j = tid; j < Mpad; j += 128) {
+    for (int j = tid; j < Mpad; j += kEpiThreads) {
         const float2 A = ml_s[j], Bp = ml2_s[j];
         const float Mx = fmaxf(A.x, Bp.x);
         const float sa = A.x == -INFINITY ? 0.f : exp2f(A.x - Mx), sb = Bp.x == -INFINITY ? 0.f : exp2f(Bp.x - Mx);
         ml_s[j] = make_float2(Mx, A.y * sa + Bp.y * sb);
         ml2_s[j] = make_float2(sa, sb);
     }
-    named_bar_sync(1, 128);
-    for (int e4 = tid; e4 < Mpad * D / 4; e4 += 128) {
+    named_bar_sync(1, kEpiThreads);
+    for (int e4 = tid; e4 < Mpad * D / 4; e4 += kEpiThreads) {
         const float2 w = ml2_s[e4 / (D / 4)];
         float4 a4 = reinterpret_cast<float4 *>(po_s)[e4];
         const float4 b4 = reinterpret_cast<const float4 *>(po2_s)[e4];
@@ -515,11 +494,11 @@ __device__ void fwd_attn_item(const FwdParams &P, int layer, int item, uint8_t *
         a4.w = a4.w * w.x + b4.w * w.y;
         reinterpret_cast<float4 *>(po_s)[e4] = a4;
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(1, kEpiThreads);
 
     bf16 *out = P.attn_out;
     if (nch == 1) {
-        for (int e = tid; e < M * D; e += 128) {
+        for (int e = tid; e < M * D; e += kEpiThreads) {
             const int j = e / D, d = e % D;
             const int r = row0 + q0 + j / grp, h = g * grp + j % grp;
             const size_t oi = (static_cast<size_t>(r) * nq + h) * D + d;
@@ -533,11 +512,11 @@ __device__ void fwd_attn_item(const FwdParams &P, int layer, int item, uint8_t *
     {
         const float4 *src4 = reinterpret_cast<const float4 *>(po_s);
         float4 *dst4 = reinterpret_cast<float4 *>(P.att_o + slot * kFwdRows * D);
-        for (int e = tid; e < M * D / 4; e += 128) dst4[e] = src4[e];
+        for (int e = tid; e < M * D / 4; e += kEpiThreads) dst4[e] = src4[e];
     }
-    for (int j = tid; j < M; j += 128) P.att_ml[slot * kFwdRows + j] = ml_s[j];
+    for (int j = tid; j < M; j += kEpiThreads) P.att_ml[slot * kFwdRows + j] = ml_s[j];
     if (tid == 0) fwd_stamp(P, ph, 8);
-    named_bar_sync(1, 128);  // every thread's partial is written; thread 0's acq_rel atomic releases them all
+    named_bar_sync(1, kEpiThreads);  // every thread's partial is written; thread 0's acq_rel atomic releases them all
     if (tid == 0) fwd_stamp(P, ph, 9);
     if (tid == 0) {
         int *cnt = &P.att_cnt[(static_cast<size_t>(b) * P.max_slices + qs) * nkv + g];
@@ -546,15 +525,76 @@ __device__ void fwd_attn_item(const FwdParams &P, int layer, int item, uint8_t *
         *last_s = last;
         fwd_stamp(P, ph, 10);
     }
-    named_bar_sync(1, 128);  // thread 0's acquire covers the reads below
+    named_bar_sync(1, kEpiThreads);  // thread 0's acquire covers the reads below
     if (!*last_s) return;
     if (tid == 0) fwd_stamp(P, ph, 11);
     // every chunk's partial for a block of rows, copied into shared memory in one burst, then merged
     // in chunk order: Mx = max m, out = sum exp2(m - Mx) o / sum exp2(m - Mx) l
     const size_t first = static_cast<size_t>(ci - ch) * nkv + g;  // the chunks of a slice are consecutive items
+    if (nch <= kRegChunks) {
+        // few chunks: one pass computes each row's chunk weights exp2(m - Mx) and denominator into
+        // shared memory (reusing the partial region) while every thread already has its o loads in
+        // flight; then each thread combines its columns in chunk order
+        constexpr int PER = kFwdRows * (D / 4) / kEpiThreads;  // float4 columns per thread
+        constexpr int GRP = PER < 2 ? PER : 2;                  // columns whose loads are in flight together
+        float *wsc = reinterpret_cast<float *>(sm);  // [kFwdRows][kRegChunks + 1]: weights, then denominator
+        for (int i0 = 0; i0 < PER; i0 += GRP) {
+            float4 o4[GRP][kRegChunks];
+#pragma unroll
+            for (int i = 0; i < GRP; ++i) {
+                const int e4 = tid + (i0 + i) * kEpiThreads, j = e4 / (D / 4), d = (e4 % (D / 4)) * 4;
+#pragma unroll
+                for (int cc = 0; cc < kRegChunks; ++cc)
+                    if (cc < nch && j < M)
+                        o4[i][cc] = __ldcg(reinterpret_cast<const float4 *>(
+                            P.att_o + ((first + static_cast<size_t>(cc) * nkv) * kFwdRows + j) * D + d));
+            }
+            if (i0 == 0) {
+                if (tid < M) {
+                    float2 ml[kRegChunks];
+#pragma unroll
+                    for (int cc = 0; cc < kRegChunks; ++cc)
+                        if (cc < nch) ml[cc] = __ldcg(&P.att_ml[(first + static_cast<size_t>(cc) * nkv) * kFwdRows + tid]);
+                    float Mx = -INFINITY;
+#pragma unroll
+                    for (int cc = 0; cc < kRegChunks; ++cc)
+                        if (cc < nch) Mx = fmaxf(Mx, ml[cc].x);
+                    float den = 0.f;
+#pragma unroll
+                    for (int cc = 0; cc < kRegChunks; ++cc)
+                        if (cc < nch) {
+                            const float sc = ml[cc].x == -INFINITY ? 0.f : exp2f(ml[cc].x - Mx);
+                            wsc[tid * (kRegChunks + 1) + cc] = sc;
+                            den += sc * ml[cc].y;
+                        }
+                    wsc[tid * (kRegChunks + 1) + kRegChunks] = den;
+                }
+                named_bar_sync(1, kEpiThreads);
+            }
+#pragma unroll
+            for (int i = 0; i < GRP; ++i) {
+                const int e4 = tid + (i0 + i) * kEpiThreads, j = e4 / (D / 4), d = (e4 % (D / 4)) * 4;
+                if (j >= M) continue;
+                float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int cc = 0; cc < kRegChunks; ++cc)
+                    if (cc < nch) {
+                        const float sc = wsc[j * (kRegChunks + 1) + cc];
+                        num.x += sc * o4[i][cc].x;
+                        num.y += sc * o4[i][cc].y;
+                        num.z += sc * o4[i][cc].z;
+                        num.w += sc * o4[i][cc].w;
+                    }
+                store_out4(out, P.q_plane, (static_cast<size_t>(row0 + q0 + j / grp) * nq + g * grp + j % grp) * D + d,
+                           num, wsc[j * (kRegChunks + 1) + kRegChunks]);
+            }
+        }
+        if (tid == 0) fwd_stamp(P, ph, 14);
+        return;
+    }
     const int rows_fit = (S::BYTES - 16) / (nch * (D * 4 + 12) + 4);
     if (rows_fit < 1) {  // more chunks than shared memory holds: merge straight from global memory
-        for (int e = tid; e < M * D; e += 128) {
+        for (int e = tid; e < M * D; e += kEpiThreads) {
             const int j = e / D, d = e % D;
             float Mx = -INFINITY;
             for (int cc = 0; cc < nch; ++cc) Mx = fmaxf(Mx, __ldcg(&P.att_ml[(first + cc * nkv) * kFwdRows + j].x));
@@ -583,17 +623,17 @@ __device__ void fwd_attn_item(const FwdParams &P, int layer, int item, uint8_t *
         const int nr = min(rc, M - j0);
         for (int cc = 0; cc < nch; ++cc) {
             const float *src = P.att_o + ((first + static_cast<size_t>(cc) * nkv) * kFwdRows + j0) * D;
-            for (int idx = tid; idx < nr * (D / 4); idx += 128)
+            for (int idx = tid; idx < nr * (D / 4); idx += kEpiThreads)
                 cp_async16(smem_u32(so + (cc * nr) * D + idx * 4), src + idx * 4, true);
         }
         cp_async_commit();
-        for (int e = tid; e < nch * nr; e += 128) {
+        for (int e = tid; e < nch * nr; e += kEpiThreads) {
             const int cc = e / nr, rr = e - cc * nr;
             sml[e] = __ldcg(&P.att_ml[(first + static_cast<size_t>(cc) * nkv) * kFwdRows + j0 + rr]);
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpiThreads);
         // per row: Mx = max m, weight of chunk cc = exp2(m_cc - Mx), denominator = sum weight * l
-        for (int rr = tid; rr < nr; rr += 128) {
+        for (int rr = tid; rr < nr; rr += kEpiThreads) {
             float Mx = -INFINITY;
             for (int cc = 0; cc < nch; ++cc) Mx = fmaxf(Mx, sml[cc * nr + rr].x);
             float den = 0.f;
@@ -606,10 +646,10 @@ __device__ void fwd_attn_item(const FwdParams &P, int layer, int item, uint8_t *
             sden[rr] = den;
         }
         cp_async_wait_all();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpiThreads);
         if (tid == 0 && j0 == 0) fwd_stamp(P, ph, 12);
         // out = sum over chunks, in order, of weight * o, over the denominator; four columns a thread
-        for (int e4 = tid; e4 < nr * (D / 4); e4 += 128) {
+        for (int e4 = tid; e4 < nr * (D / 4); e4 += kEpiThreads) {
             const int rr = e4 / (D / 4), d = (e4 % (D / 4)) * 4, j = j0 + rr;
             float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int cc = 0; cc < nch; ++cc) {
@@ -620,23 +660,10 @@ __device__ void fwd_attn_item(const FwdParams &P, int layer, int item, uint8_t *
                 num.z += sc * o4.z;
                 num.w += sc * o4.w;
             }
-            const float den = sden[rr];
-            const int r = row0 + q0 + j / grp, h = g * grp + j % grp;
-            const size_t oi = (static_cast<size_t>(r) * nq + h) * D + d;
-            const Bf16Pair p0 = split_bf16(num.x / den), p1 = split_bf16(num.y / den);
-            const Bf16Pair p2 = split_bf16(num.z / den), p3 = split_bf16(num.w / den);
-            __nv_bfloat162 hi01, hi23, lo01, lo23;
-            hi01.x = p0.hi; hi01.y = p1.hi; hi23.x = p2.hi; hi23.y = p3.hi;
-            lo01.x = p0.lo; lo01.y = p1.lo; lo23.x = p2.lo; lo23.y = p3.lo;
-            uint2 hv, lv;
-            hv.x = *reinterpret_cast<uint32_t *>(&hi01);
-            hv.y = *reinterpret_cast<uint32_t *>(&hi23);
-            lv.x = *reinterpret_cast<uint32_t *>(&lo01);
-            lv.y = *reinterpret_cast<uint32_t *>(&lo23);
-            *reinterpret_cast<uint2 *>(out + oi) = hv;
-            *reinterpret_cast<uint2 *>(out + oi + P.q_plane) = lv;
+            store_out4(out, P.q_plane, (static_cast<size_t>(row0 + q0 + j / grp) * nq + g * grp + j % grp) * D + d,
+                       num, sden[rr]);
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpiThreads);
         if (tid == 0 && j0 == 0) fwd_stamp(P, ph, 13);
     }
     if (tid == 0) fwd_stamp(P, ph, 14);
@@ -644,20 +671,60 @@ __device__ void fwd_attn_item(const FwdParams &P, int layer, int item, uint8_t *
 
 
 // ------------------------------------------------------------------ the kernel
+// Shared memory: a ring of SA weight tiles (16 KB, TMA destination), then one region that
+// attention uses whole during an attention phase and that otherwise holds a 64 KB ring of SB
+// activation tiles followed by the epilogue's staging area. (Attention runs only after every
+// activation tile of the phase before it was consumed, and the next phase's activations load only
+// after every attention item is done.) Tensor memory (all 512 columns): two accumulators of NC
+// columns, then NT weight-tile slots of 32 columns that the MMA reads its A operand from. A weight
+// tile moves shared -> tensor memory (tcgen05.cp) as soon as it lands, so the shared slot turns
+// over at copy speed and up to NT tiles wait on chip for their activations.
 template <int N, int D>
 struct FwdShape {
     using GS = GemmShape<N>;
-    static constexpr int STAGE = GS::STAGE_BYTES;
-    static constexpr int ATT_RAW = FwdAttnSmem<D>::BYTES > 32 * 128 * 4 ? FwdAttnSmem<D>::BYTES : 32 * 128 * 4;
-    static constexpr int ATT = (ATT_RAW + 1023) & ~1023;  // attention, or the epilogue's 32-row staging
-    static constexpr int BUDGET = kFwdSmemLimit - ATT - 1024 - 3072;  // alignment slack, static shared memory
-    static constexpr int STAGES_RAW = BUDGET / STAGE;
-    static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
-    static constexpr int NC = N < 32 ? 32 : N;  // TMEM columns per accumulator
-    static constexpr int TMEM_COLS = 2 * NC;
-    static constexpr int SMEM_BYTES = STAGES * STAGE + ATT + 1024;
-    static_assert(STAGES >= 2, "pipeline too shallow");
+    static constexpr int A_TILE = GS::A_BYTES;   // 16 KB
+    static constexpr int B_TILE = GS::B_BYTES;   // hi and lo planes, N rows x 64
+    static constexpr int TOTAL = kFwdSmemLimit - 1024 - 3072;  // alignment slack, static shared memory
+    static constexpr int SA = 7;
+    static constexpr int X_OFF = SA * A_TILE;
+    static constexpr int X_BYTES = (TOTAL - X_OFF) & ~1023;
+    static constexpr int B_RING = 65536;
+    static constexpr int SB = B_RING / B_TILE;
+    static constexpr int B_OFF = X_OFF;
+    static constexpr int STAGE_OFF = X_OFF + B_RING;
+    static constexpr int STAGE_BYTES = X_BYTES - B_RING;  // epilogue staging
+    static constexpr int ATT_OFF = X_OFF;
+    // An accumulator holds the hi-plane product in columns [0, N) and the lo-plane product in
+    // [N, 2N); the epilogue adds them. Up to N = 64 one MMA of width 2N covers both planes (the
+    // activation tile stores the lo rows right after the hi rows), which halves the MMA count per
+    // weight byte; at N = 128 each plane is its own MMA and a single accumulator fits beside the
+    // weight slots.
+    static constexpr bool COMBINED = N <= 64;
+    static constexpr int NC = 2 * N;                  // TMEM columns per accumulator
+    static constexpr int ACC = COMBINED ? 2 : 1;      // accumulators (ping-pong between segments)
+    static constexpr uint32_t IDESC = idesc_bf16(128, COMBINED ? 2 * N : N);
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int NT = (TMEM_COLS - ACC * NC) / 32;
+    static constexpr int SMEM_BYTES = X_OFF + X_BYTES + 1024;
+    static_assert(FwdAttnSmem<D>::BYTES <= X_BYTES, "attention must fit the shared region");
+    static_assert(STAGE_BYTES >= 32 * 128 * 4, "staging holds 32 rows of a tile");
+    static_assert(SB >= 2 && NT >= 4, "pipeline too shallow");
 };
+
+// tcgen05 forms for a weight tile staged in tensor memory: copy 128 rows x 32 bytes (one 16-wide
+// k slice) from shared memory through a matrix descriptor, and an MMA that reads A from TMEM.
+__device__ __forceinline__ void tc_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 
 // Shared state the epilogue warps use.
 struct FwdEpiCtx {
@@ -667,12 +734,36 @@ struct FwdEpiCtx {
     int *flag, *last;
     uint32_t tmem;
     int *status;
-    int R, rows_cap, c, G, stage_bytes, nc;
+    int R, rows_cap, c, G, stage_bytes, nc, n, acc_slots;
 };
 
-// The epilogue warps' part of one GEMM phase of kind EK: every segment this CTA holds, in
-// order. Whole tiles go accumulator -> staging -> a warp per row; split tiles park their partial
-// and the last holder to arrive adds every holder's partial in CTA order. Returns false on abort.
+// Count one finished tile of phase p; the last tile of the LM head publishes the argmax.
+template <int EK>
+__device__ __forceinline__ void fwd_tile_done(const FwdParams &P, const FwdEpiCtx &E, int p, int tiles) {
+    const int tid = threadIdx.x;
+    named_bar_sync(1, kEpiThreads);
+    if (tid == 0) {
+        const int prev = atom_add_acq_rel_gpu(&P.done[p], 1);
+        *E.last = EK == EPI_LMHEAD && prev == tiles - 1;
+    }
+    named_bar_sync(1, kEpiThreads);
+    if constexpr (EK == EPI_LMHEAD) {
+        if (*E.last) {  // every tile's row maxima are in: publish the argmax
+            const GemmArgs &a = P.ga[EK];
+            for (int r = tid; r < E.R; r += kEpiThreads) {
+                const unsigned long long k = atomicAdd(&a.keys[r], 0ull);
+                a.argmax_out[r] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k & 0xffffffffull));
+            }
+        }
+    }
+}
+
+// The epilogue warps' part of one GEMM phase of kind EK. First every segment this CTA holds,
+// in order: a whole tile goes accumulator -> staging -> a warp per row; a split tile's
+// partial is parked in global memory and the holder's arrival counted. Then, for the split
+// tiles where this CTA arrived last, every holder's partial (and, for a residual epilogue,
+// the old residual rows) is copied into shared memory in one burst and added in holder (CTA)
+// order. Returns false on abort.
 template <int EK>
 __device__ bool fwd_gemm_epi(const FwdParams &P, const FwdEpiCtx &E, const EpiLayer &el, int p, int gi, int &q,
                              bool first_phase_seg_stamp) {
@@ -694,7 +785,7 @@ __device__ bool fwd_gemm_epi(const FwdParams &P, const FwdEpiCtx &E, const EpiLa
             }
             es.rstd[tid] = rsqrtf(sum / static_cast<float>(a.hidden) + a.eps);
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpiThreads);
     }
     const FwdGemm gm = P.g[gi];
     const int *hoff = P.hold + P.hold_base[gi];
@@ -703,49 +794,52 @@ __device__ bool fwd_gemm_epi(const FwdParams &P, const FwdEpiCtx &E, const EpiLa
     SegRange sr(gm, c, G);
     int t, kb0, kb1;
     bool first_seg = first_phase_seg_stamp;
+    int pend_t[2], npend = 0;  // split tiles this CTA reduces (at most its first and last segment)
     while (sr.next(t, kb0, kb1)) {
-        const int acc = q & 1;
-        if (tid == 0) *E.flag = fwd_bar_wait(P, E.status, &E.acc_full[acc], (q >> 1) & 1);
-        named_bar_sync(1, 128);
+        const int acc = q % E.acc_slots;
+        if (tid == 0) *E.flag = fwd_bar_wait(P, E.status, &E.acc_full[acc], (q / E.acc_slots) & 1);
+        named_bar_sync(1, kEpiThreads);
         const int go = *E.flag;
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpiThreads);
         if (!go) return false;
         if (tid == 0 && first_seg) fwd_stamp(P, p, 4);
         tc_fence_after();
         const int h0 = __ldg(&hoff[t]), nh = __ldg(&hoff[t + 1]) - h0;
         const uint32_t tacc = E.tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(acc * E.nc);
-        bool finish = false;
         float v[32];
         if (nh == 1) {
             for (int c0 = 0; c0 < R; c0 += 32) {
-                tmem_ld32(tacc + c0, v);
+                if (warp < 4) {
+                    acc_load(tacc, c0, E.n, v);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c0 + j < R) E.stage[j * 128 + tid] = v[j];
-                named_bar_sync(1, 128);
-                for (int r = c0 + warp; r < min(R, c0 + 32); r += 4) {
+                    for (int j = 0; j < 32; ++j)
+                        if (c0 + j < R) E.stage[j * 128 + tid] = v[j];
+                }
+                named_bar_sync(1, kEpiThreads);
+                for (int r = c0 + warp; r < min(R, c0 + 32); r += kEpiWarps) {
                     float x[4];
 #pragma unroll
                     for (int i = 0; i < 4; ++i) x[i] = E.stage[(r - c0) * 128 + lane + 32 * i];
                     epi_row<EK>(a, el, es, t, r, lane, x);
                 }
-                named_bar_sync(1, 128);
+                named_bar_sync(1, kEpiThreads);
             }
             tc_fence_before();
-            named_bar_sync(1, 128);
+            named_bar_sync(1, kEpiThreads);
             if (tid == 0) mbar_arrive(&E.acc_empty[acc]);
-            finish = true;
+            fwd_tile_done<EK>(P, E, p, gm.tiles);
         } else {
             const int my_slot = 2 * c + (t == my_first_tile ? 0 : 1);
             float *pp = P.part + static_cast<size_t>(my_slot) * rows_cap * 128;
-            for (int c0 = 0; c0 < R; c0 += 32) {
-                tmem_ld32(tacc + c0, v);
+            if (warp < 4)
+                for (int c0 = 0; c0 < R; c0 += 32) {
+                    acc_load(tacc, c0, E.n, v);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c0 + j < R) pp[static_cast<size_t>(c0 + j) * 128 + tid] = v[j];
-            }
+                    for (int j = 0; j < 32; ++j)
+                        if (c0 + j < R) pp[static_cast<size_t>(c0 + j) * 128 + tid] = v[j];
+                }
             tc_fence_before();
-            named_bar_sync(1, 128);  // thread 0's acq_rel atomic releases every thread's partial
+            named_bar_sync(1, kEpiThreads);  // thread 0's acq_rel atomic releases every thread's partial
             if (tid == 0) {
                 mbar_arrive(&E.acc_empty[acc]);
                 const int last = atom_add_acq_rel_gpu(&P.tile_cnt[gi * P.tile_stride + t], 1) == nh - 1;
@@ -753,55 +847,53 @@ __device__ bool fwd_gemm_epi(const FwdParams &P, const FwdEpiCtx &E, const EpiLa
                 *E.last = last;
                 if (first_seg) fwd_stamp(P, p, 5);
             }
-            named_bar_sync(1, 128);
-            if (*E.last) {
-                // every holder's partial for a block of rows, one burst into shared memory, then
-                // added in holder (CTA) order (thread 0's acquire covers these reads)
-                const int rc = min(32, E.stage_bytes / (nh * 512));
-                for (int r0 = 0; r0 < R; r0 += rc) {
-                    const int nr = min(rc, R - r0);
-                    for (int h = 0; h < nh; ++h) {
-                        const float *src = P.part + (static_cast<size_t>(__ldg(&hslot[h0 + h])) * rows_cap + r0) * 128;
-                        for (int idx = tid; idx < nr * 32; idx += 128)
-                            cp_async16(smem_u32(E.stage + (h * nr + (idx >> 5)) * 128 + (idx & 31) * 4),
-                                       src + (idx >> 5) * 128 + (idx & 31) * 4, true);
-                    }
-                    cp_async_commit();
-                    cp_async_wait_all();
-                    named_bar_sync(1, 128);
-                    if (tid == 0 && r0 == 0 && first_seg) fwd_stamp(P, p, 6);
-                    for (int r = r0 + warp; r < r0 + nr; r += 4) {
-                        float x[4] = {0.f, 0.f, 0.f, 0.f};
-                        for (int h = 0; h < nh; ++h) {
-                            const float *src = E.stage + (h * nr + (r - r0)) * 128 + lane;
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) x[i] += src[32 * i];
-                        }
-                        epi_row<EK>(a, el, es, t, r, lane, x);
-                    }
-                    named_bar_sync(1, 128);
-                }
-                finish = true;
-            }
-        }
-        if (finish) {
-            named_bar_sync(1, 128);
-            if (tid == 0) {
-                const int prev = atom_add_acq_rel_gpu(&P.done[p], 1);
-                *E.last = EK == EPI_LMHEAD && prev == gm.tiles - 1;
-            }
-            named_bar_sync(1, 128);
-            if constexpr (EK == EPI_LMHEAD) {
-                if (*E.last) {  // every tile's row maxima are in: publish the argmax
-                    for (int r = tid; r < R; r += 128) {
-                        const unsigned long long k = atomicAdd(&a.keys[r], 0ull);
-                        a.argmax_out[r] = static_cast<int>(0xffffffffu - static_cast<uint32_t>(k & 0xffffffffull));
-                    }
-                }
-            }
+            named_bar_sync(1, kEpiThreads);
+            if (*E.last) pend_t[npend++] = t;
+            named_bar_sync(1, kEpiThreads);
         }
         ++q;
         first_seg = false;
+    }
+    for (int k = 0; k < npend; ++k) {  // thread 0's acquire (the arrival atomic) covers these reads
+        t = pend_t[k];
+        const int h0 = __ldg(&hoff[t]), nh = __ldg(&hoff[t + 1]) - h0;
+        constexpr int extra = EK == EPI_RESID ? 1 : 0;  // the old residual rows ride along
+        const int rc = min(32, E.stage_bytes / ((nh + extra) * 512));
+        for (int r0 = 0; r0 < R; r0 += rc) {
+            const int nr = min(rc, R - r0);
+            for (int h = 0; h < nh; ++h) {
+                const float *src = P.part + (static_cast<size_t>(__ldg(&hslot[h0 + h])) * rows_cap + r0) * 128;
+                for (int idx = tid; idx < nr * 32; idx += kEpiThreads)
+                    cp_async16(smem_u32(E.stage + (h * nr + (idx >> 5)) * 128 + (idx & 31) * 4),
+                               src + (idx >> 5) * 128 + (idx & 31) * 4, true);
+            }
+            if constexpr (EK == EPI_RESID) {
+                for (int idx = tid; idx < nr * 32; idx += kEpiThreads) {
+                    const int rr = idx >> 5, q4 = idx & 31;
+                    const bool in = t * 128 + q4 * 4 < a.n_out;  // features past the hidden size read as 0
+                    cp_async16(smem_u32(E.stage + (nh * nr + rr) * 128 + q4 * 4),
+                               in ? a.x + static_cast<size_t>(r0 + rr) * a.hidden + t * 128 + q4 * 4 : a.x, in);
+                }
+            }
+            cp_async_commit();
+            cp_async_wait_all();
+            named_bar_sync(1, kEpiThreads);
+            if (tid == 0 && r0 == 0 && k == 0 && first_phase_seg_stamp) fwd_stamp(P, p, 6);
+            for (int r = r0 + warp; r < r0 + nr; r += kEpiWarps) {
+                float x[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int h = 0; h < nh; ++h) {
+                    const float *src = E.stage + (h * nr + (r - r0)) * 128 + lane;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) x[i] += src[32 * i];
+                }
+                if constexpr (EK == EPI_RESID)
+                    epi_resid_row(a, el, t, r, lane, x, E.stage + (nh * nr + (r - r0)) * 128);
+                else
+                    epi_row<EK>(a, el, es, t, r, lane, x);
+            }
+            named_bar_sync(1, kEpiThreads);
+        }
+        fwd_tile_done<EK>(P, E, p, gm.tiles);
     }
     return true;
 }
@@ -840,11 +932,14 @@ template <int N, int D>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams P) {
     using F = FwdShape<N, D>;
     using GS = GemmShape<N>;
-    constexpr int ST = F::STAGES;
+    constexpr int SA = F::SA, SB = F::SB, NT = F::NT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *att = smem + ST * GS::STAGE_BYTES;
-    __shared__ __align__(8) uint64_t fullA[ST], fullB[ST], empty[ST], acc_full[2], acc_empty[2], fin_bar;
+    uint8_t *sB = smem + F::B_OFF;
+    uint8_t *att = smem + F::ATT_OFF;
+    uint8_t *stage = smem + F::STAGE_OFF;
+    __shared__ __align__(8) uint64_t fullA[SA], emptyA[SA], fullB[SB], emptyB[SB], tfree[NT], tcopied[NT];
+    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], fin_bar, fin_bar2;
     __shared__ uint32_t tmem_s;
     __shared__ EpiSmem es;
     __shared__ int page_s[kFwdChunk + 1];
@@ -853,23 +948,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int c = blockIdx.x, G = P.grid, nL = P.n_layers;
     const int n_ph = 5 * nL + 1;
-    const int nst = P.ring >= 1 && P.ring <= ST ? P.ring : ST;
+    const int nsa = P.ring >= 3 && P.ring <= SA ? P.ring : SA;  // weight-ring slots in use
     int *status = P.ga[EPI_QKV].status;
 
     if (tid == 0) {
-        for (int s = 0; s < ST; ++s) {
+        for (int s = 0; s < SA; ++s) {
             mbar_init(&fullA[s], 1);
+            mbar_init(&emptyA[s], 1);
+        }
+        for (int s = 0; s < SB; ++s) {
             mbar_init(&fullB[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&emptyB[s], 1);
+        }
+        for (int s = 0; s < NT; ++s) {
+            mbar_init(&tfree[s], 1);
+            mbar_init(&tcopied[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&acc_full[s], 1);
             mbar_init(&acc_empty[s], 1);
         }
         mbar_init(&fin_bar, 1);
+        mbar_init(&fin_bar2, 1);
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tmem_alloc(&tmem_s, F::TMEM_COLS);
         tmem_relinquish();
     }
@@ -880,20 +983,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     pdl_trigger();
     pdl_wait();
 
-    if (warp == 4) {
-        // ---------------- weight producer: never waits on another CTA. It loads the ring in
-        // consumption order (the tensor maps and row coordinate of a segment are resolved once per
-        // segment) and optionally keeps a window of l2_ahead further k-blocks in flight into L2.
+    if (warp == kWarpProducerA) {
+        // ---------------- weight producer: never waits on another CTA. It loads the weight ring in
+        // consumption order; the tensor maps and row coordinate of a segment are resolved once per
+        // segment.
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             RingPos rp;
-            KCursor pf(P, c, G);
-            const bool pf_on = P.l2_ahead > 0;
-            if (pf_on)
-                for (int i = 0; i < P.l2_ahead && pf.valid(); ++i, pf.advance(P)) {
-                    const int kind = pf.kind();
-                    fwd_prefetch_a(fwd_epi(kind), fwd_wmap(P, kind, pf.p / 5), P.ga[fwd_epi(kind)], pf.tile(), pf.kc());
-                }
             bool ok = true;
             for (int p = 0; p < n_ph && ok; ++p) {
                 const int kind = fwd_kind(p, nL);
@@ -919,28 +1015,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                         row = t * 64;
                     }
                     for (int kc = kb0 * 64; kc < kb1 * 64; kc += 64) {
-                        if (!fwd_bar_wait(P, status, &empty[rp.s], rp.ph ^ 1)) {
+                        if (!fwd_bar_wait(P, status, &emptyA[rp.s], rp.ph ^ 1)) {
                             ok = false;
                             break;
                         }
-                        uint8_t *dst = smem + rp.s * GS::STAGE_BYTES;
-                        mbar_arrive_expect_tx(&fullA[rp.s], GS::A_BYTES);
+                        uint8_t *dst = smem + rp.s * F::A_TILE;
+                        mbar_arrive_expect_tx(&fullA[rp.s], F::A_TILE);
                         tma_load_2d_hint(dst, m0, &fullA[rp.s], kc, row, pol);
-                        if (m1) tma_load_2d_hint(dst + GS::A_BYTES / 2, m1, &fullA[rp.s], kc, row, pol);
-                        if (pf_on && pf.valid()) {
-                            const int pk = pf.kind();
-                            fwd_prefetch_a(fwd_epi(pk), fwd_wmap(P, pk, pf.p / 5), P.ga[fwd_epi(pk)], pf.tile(), pf.kc());
-                            pf.advance(P);
-                        }
-                        rp.next(nst);
+                        if (m1) tma_load_2d_hint(dst + F::A_TILE / 2, m1, &fullA[rp.s], kc, row, pol);
+                        rp.next(nsa);
                     }
                 }
                 fwd_stamp(P, p, 3);
             }
-            rp.drain(fullA, nst);  // own copies in flight
+            rp.drain(fullA, nsa);  // own copies in flight
         }
         __syncwarp();
-    } else if (warp == 6) {
+    } else if (warp == kWarpProducerB) {
         // ---------------- activation producer: waits for the previous phase, then loads B
         if (lane == 0) {
             RingPos rp;
@@ -958,56 +1049,96 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                 int t, kb0, kb1;
                 while (ok && sr.next(t, kb0, kb1)) {
                     for (int kc = kb0 * 64; kc < kb1 * 64; kc += 64) {
-                        if (!fwd_bar_wait(P, status, &empty[rp.s], rp.ph ^ 1)) {
+                        if (!fwd_bar_wait(P, status, &emptyB[rp.s], rp.ph ^ 1)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&fullB[rp.s], GS::B_BYTES);
-                        tma_load_3d(smem + rp.s * GS::STAGE_BYTES + GS::A_BYTES, tb, &fullB[rp.s], kc, 0, 0);
-                        rp.next(nst);
+                        mbar_arrive_expect_tx(&fullB[rp.s], F::B_TILE);
+                        tma_load_3d(sB + rp.s * F::B_TILE, tb, &fullB[rp.s], kc, 0, 0);
+                        rp.next(SB);
                     }
                 }
             }
-            rp.drain(fullB, nst);
+            rp.drain(fullB, SB);
         }
         __syncwarp();
-    } else if (warp == 5) {
-        // ---------------- MMA issuer: two TMEM accumulators, one per segment in flight
+    } else if (warp == kWarpCopier) {
+        // ---------------- copier: each landed weight tile moves into the next TMEM slot once the
+        // MMAs that last read that slot are done; the shared slot is free as soon as the copy is.
+        // It never waits on activations, so across a phase hand-off the weights keep streaming.
         if (lane == 0) {
-            RingPos rp;
+            int total = 0;  // this CTA's k-blocks over every GEMM phase
+            for (int p = 0; p < n_ph; ++p) {
+                const int kind = fwd_kind(p, nL);
+                if (kind == FP_ATTN) continue;
+                const FwdGemm &g = P.g[fwd_gemm_index(kind)];
+                const int U = g.tiles * g.kblocks;
+                total += unit_begin(c + 1, U, G) - unit_begin(c, U, G);
+            }
+            const uint32_t sa0 = smem_u32(smem), tA = tmem + F::ACC * F::NC;
+            RingPos ca, ta;
+            for (int it = 0; it < total; ++it) {
+                if (!fwd_bar_wait(P, status, &fullA[ca.s], ca.ph) || !fwd_bar_wait(P, status, &tfree[ta.s], ta.ph ^ 1))
+                    break;
+                tc_fence_after();
+                const uint64_t ad = sw128_desc(sa0 + ca.s * F::A_TILE);
+                const uint32_t dst = tA + ta.s * 32;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tc_cp_128x256b(dst + 8 * k, ad + 2 * k);
+                umma_commit(&tcopied[ta.s]);
+                umma_commit(&emptyA[ca.s]);
+                ca.next(nsa);
+                ta.next(NT);
+            }
+            umma_commit(&fin_bar);  // every copy issued above has completed once this fires
+            mbar_wait(&fin_bar, 0);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        // ---------------- MMA issuer: A from the TMEM slot the copier filled, B from the
+        // activation ring; two TMEM accumulators, one per segment in flight
+        if (lane == 0) {
+            const uint32_t sb0 = smem_u32(sB), tA = tmem + F::ACC * F::NC;
+            RingPos mt, mb;
             int q = 0;
             bool ok = true;
-            const uint32_t s0 = smem_u32(smem);
             for (int p = 0; p < n_ph && ok; ++p) {
                 const int kind = fwd_kind(p, nL);
                 if (kind == FP_ATTN) continue;
                 SegRange sr(P.g[fwd_gemm_index(kind)], c, G);
                 int t, kb0, kb1;
                 while (ok && sr.next(t, kb0, kb1)) {
-                    const int acc = q & 1;
-                    if (q >= 2 && !fwd_bar_wait(P, status, &acc_empty[acc], ((q >> 1) - 1) & 1)) {
+                    const int acc = q % F::ACC, use = q / F::ACC;
+                    if (use >= 1 && !fwd_bar_wait(P, status, &acc_empty[acc], (use - 1) & 1)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t d = tmem + static_cast<uint32_t>(acc * F::NC);
                     for (int kb = kb0; kb < kb1; ++kb) {
-                        if (!fwd_bar_wait(P, status, &fullA[rp.s], rp.ph) || !fwd_bar_wait(P, status, &fullB[rp.s], rp.ph)) {
+                        if (!fwd_bar_wait(P, status, &tcopied[mt.s], mt.ph) ||
+                            !fwd_bar_wait(P, status, &fullB[mb.s], mb.ph)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t sa = s0 + rp.s * GS::STAGE_BYTES;
-                        const uint64_t ad = sw128_desc(sa);
-                        const uint64_t bh = sw128_desc(sa + GS::A_BYTES);
-                        const uint64_t bl = sw128_desc(sa + GS::A_BYTES + GS::B_PLANE);
+                        const uint32_t a_t = tA + mt.s * 32;
+                        const uint64_t bh = sw128_desc(sb0 + mb.s * F::B_TILE);
+                        const uint64_t bl = sw128_desc(sb0 + mb.s * F::B_TILE + GS::B_PLANE);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            umma_bf16(d, ad + 2 * k, bh + 2 * k, GS::IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
-                            umma_bf16(d, ad + 2 * k, bl + 2 * k, GS::IDESC, 1u);
+                            const uint32_t accum = (kb > kb0 || k > 0) ? 1u : 0u;
+                            if constexpr (F::COMBINED) {  // both planes: rows 0..N-1 hi, N..2N-1 lo
+                                umma_bf16_tmem_a(d, a_t + 8 * k, bh + 2 * k, F::IDESC, accum);
+                            } else {
+                                umma_bf16_tmem_a(d, a_t + 8 * k, bh + 2 * k, F::IDESC, accum);
+                                umma_bf16_tmem_a(d + N, a_t + 8 * k, bl + 2 * k, F::IDESC, accum);
+                            }
                         }
-                        umma_commit(&empty[rp.s]);
-                        rp.next(nst);
+                        umma_commit(&emptyB[mb.s]);
+                        umma_commit(&tfree[mt.s]);
+                        mt.next(NT);
+                        mb.next(SB);
                     }
                     if (!ok) break;
                     umma_commit(&acc_full[acc]);
@@ -1015,12 +1146,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                 }
                 fwd_stamp(P, p, 1);
             }
-            umma_commit(&fin_bar);  // every MMA issued above has completed once this fires
-            mbar_wait(&fin_bar, 0);
+            umma_commit(&fin_bar2);  // every MMA issued above has completed once this fires
+            mbar_wait(&fin_bar2, 0);
         }
         __syncwarp();
     } else {
-        // ---------------- warps 0-3: epilogues and attention
+        // ---------------- warps 0-7: epilogues and attention
         int R = *P.ga[EPI_QKV].nrows;
         if (R > N) {
             if (tid == 0) set_status(status, SDV_ERR_ARG);
@@ -1031,7 +1162,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         E.acc_full = acc_full;
         E.acc_empty = acc_empty;
         E.es = &es;
-        E.stage = reinterpret_cast<float *>(att);
+        E.stage = reinterpret_cast<float *>(stage);
         E.flag = &flag_s;
         E.last = &last_s;
         E.tmem = tmem;
@@ -1040,16 +1171,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         E.rows_cap = rows_cap;
         E.c = c;
         E.G = G;
-        E.stage_bytes = F::ATT;
+        E.stage_bytes = F::STAGE_BYTES;
         E.nc = F::NC;
+        E.n = N;
+        E.acc_slots = F::ACC;
         int q = 0;
         for (int p = 0; p < n_ph; ++p) {
             const int kind = fwd_kind(p, nL), layer = p / 5;
             if (p > 0) {  // the previous phase's outputs, and transitively every earlier phase's
                 if (tid == 0) flag_s = fwd_count_wait(P, status, &P.done[p - 1], fwd_target(P, fwd_kind(p - 1, nL)));
-                named_bar_sync(1, 128);
+                named_bar_sync(1, kEpiThreads);
                 const int go = flag_s;
-                named_bar_sync(1, 128);  // every thread has read the flag before it is reused
+                named_bar_sync(1, kEpiThreads);  // every thread has read the flag before it is reused
                 if (!go) break;
             }
             if (kind == FP_ATTN) {
@@ -1057,7 +1190,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
                 const int n_it = fwd_target(P, FP_ATTN);
                 for (int i = c; i < n_it; i += G) {
                     fwd_attn_item<D>(P, layer, i, att, page_s, &last_s, i == c ? p : -1);
-                    named_bar_sync(1, 128);
+                    named_bar_sync(1, kEpiThreads);
                     if (tid == 0) red_release_gpu(&P.done[p], 1);
                 }
                 if (tid == 0) fwd_stamp(P, p, 2);
@@ -1086,7 +1219,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, F::TMEM_COLS);
     }

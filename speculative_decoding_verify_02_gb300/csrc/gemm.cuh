@@ -69,9 +69,13 @@ struct GemmShape {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES_RAW = (104 * 1024) / STAGE_BYTES;  // two CTAs per SM
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-    static constexpr int TMEM_COLS = N < 32 ? 32 : N;
+    // The hi and lo planes are adjacent in the B stage (N rows each), so one MMA of width 2N
+    // covers both: hi product in accumulator columns [0, N), lo product in [N, 2N). One MMA per
+    // 16-wide k step instead of two: the tensor core's cost is per instruction at these widths.
+    static constexpr int TMEM_COLS = 2 * N < 32 ? 32 : 2 * N;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
     static constexpr uint32_t IDESC = idesc_bf16(128, N);
+    static constexpr uint32_t IDESC2 = idesc_bf16(128, 2 * N);
     static_assert(STAGES >= 2, "pipeline too shallow");
     static_assert(B_PLANE % 1024 == 0, "B planes must keep 1024-byte alignment");
 };
@@ -172,15 +176,16 @@ __device__ __forceinline__ void epi_qkv_row(const GemmArgs &a, const EpiLayer &e
     }
 }
 
+// xs: the row's 128 residual values already staged in shared memory, or nullptr to read them
 __device__ __forceinline__ void epi_resid_row(const GemmArgs &a, const EpiLayer &el, int tile, int r, int lane,
-                                              float (&x)[4]) {
+                                              float (&x)[4], const float *xs = nullptr) {
     float sq = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int F = tile * 128 + lane + 32 * i;
         if (F < a.n_out) {
             const size_t o = static_cast<size_t>(r) * a.hidden + F;
-            const float xn = __ldcg(&a.x[o]) + x[i];
+            const float xn = (xs ? xs[lane + 32 * i] : __ldcg(&a.x[o])) + x[i];
             a.x[o] = xn;
             const Bf16Pair pr = split_bf16(xn * __bfloat162float(el.g_next[F]));
             a.xb[o] = pr.hi;
@@ -237,6 +242,22 @@ __device__ __forceinline__ void epi_row(const GemmArgs &a, const EpiLayer &el, c
     else if constexpr (KIND == EPI_RESID) epi_resid_row(a, el, tile, r, lane, x);
     else if constexpr (KIND == EPI_SWIGLU) epi_swiglu_row(a, es.rstd[r], tile, r, lane, x);
     else epi_lmhead_row(a, es.rstd[r], tile, r, lane, x);
+}
+
+// Accumulator rows c0..c0+31 of this warp's 32 output features: hi-plane product (columns
+// [0, n)) plus lo-plane product (columns [n, 2n)).
+__device__ __forceinline__ void acc_load(uint32_t base, int c0, int n, float (&v)[32]) {
+    if (n == 16) {  // one 32-column load holds both halves
+        tmem_ld32(base, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] += v[16 + j];
+        return;
+    }
+    float w[32];
+    tmem_ld32(base + c0, v);
+    tmem_ld32(base + n + c0, w);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] += w[j];
 }
 
 // ------------------------------------------------------------------ kernel
@@ -367,13 +388,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 }
                 tc_fence_after();
                 const uint64_t ad = sw128_desc(smem_u32(smem + s * S::STAGE_BYTES));
-                const uint64_t bh = sw128_desc(smem_u32(smem + s * S::STAGE_BYTES + S::A_BYTES));
-                const uint64_t bl = sw128_desc(smem_u32(smem + s * S::STAGE_BYTES + S::A_BYTES + S::B_PLANE));
+                const uint64_t bd = sw128_desc(smem_u32(smem + s * S::STAGE_BYTES + S::A_BYTES));  // hi rows, then lo
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    umma_bf16(tmem, ad + 2 * k, bh + 2 * k, S::IDESC, (i > 0 || k > 0) ? 1u : 0u);
-                    umma_bf16(tmem, ad + 2 * k, bl + 2 * k, S::IDESC, 1u);
-                }
+                for (int k = 0; k < 4; ++k) umma_bf16(tmem, ad + 2 * k, bd + 2 * k, S::IDESC2, (i > 0 || k > 0) ? 1u : 0u);
                 umma_commit(&empty_bar[s]);
             }
             umma_commit(&accum_bar);
@@ -406,7 +423,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         const int f = threadIdx.x;
         float v[32];
         for (int c0 = 0; c0 < R; c0 += 32) {
-            tmem_ld32(taddr + c0, v);
+            acc_load(taddr, c0, N, v);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
                 if (c0 + j < R) red[(c0 + j) * 128 + f] = v[j];

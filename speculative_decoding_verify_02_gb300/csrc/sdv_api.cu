@@ -128,7 +128,6 @@ struct sdv_ctx {
     int *fwd_hold = nullptr;         // device table of split-tile holders (FwdParams::hold)
     int fwd_hold_base[5] = {0, 0, 0, 0, 0};
     std::vector<int> fwd_hold_host;
-    int fwd_l2_ahead = 16;                    // SDV_L2_AHEAD overrides
     int fwd_ring = 0;                         // ring stages in use, 0 = all; SDV_RING overrides
     unsigned long long *fwd_trace = nullptr;  // caller's timeline buffer, or nullptr
     std::vector<CUtensorMap> fwd_tm_host;
@@ -696,7 +695,6 @@ int launch_fwd(sdv_ctx *ctx, int nidx, int32_t *d_argmax, float *d_logits, cudaS
     P.part = ctx->fwd_part;
     P.abort_flag = ctx->fwd_abort;
     P.trace = ctx->fwd_trace;
-    P.l2_ahead = ctx->fwd_l2_ahead;
     P.hold = ctx->fwd_hold;
     for (int i = 0; i < 5; ++i) P.hold_base[i] = ctx->fwd_hold_base[i];
     P.ring = ctx->fwd_ring;
@@ -836,17 +834,15 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
         const char *ev = std::getenv("SDV_FORWARD");
         if (!(ev && std::strcmp(ev, "persistent") == 0)) ctx->use_fwd = false;
         if (c->page_size & (c->page_size - 1)) ctx->use_fwd = false;  // page index by shift
-        const char *la = std::getenv("SDV_L2_AHEAD");
-        if (la) ctx->fwd_l2_ahead = std::max(0, std::atoi(la));
         const char *rg = std::getenv("SDV_RING");
         if (rg) ctx->fwd_ring = std::max(0, std::atoi(rg));
         // the kernel's unit arithmetic is 32-bit, and a split tile's partials must fit its staging region
-        const int att = D == 128 ? FwdShape<16, 128>::ATT : FwdShape<16, 64>::ATT;
+        const int att = D == 128 ? FwdShape<128, 128>::STAGE_BYTES : FwdShape<128, 64>::STAGE_BYTES;
         for (int i = 0; i < 5; ++i) {
             const long long U = static_cast<long long>(ctx->plan[i].tiles) * ctx->plan[i].k_blocks;
             if (U * (sms + 1) >= (1ll << 31)) ctx->use_fwd = false;
             const int mh = max_holders(ctx->plan[i].tiles, ctx->plan[i].k_blocks, sms);
-            if (mh > kFwdMaxHolders || mh * 512 > att) ctx->use_fwd = false;
+            if (mh > kFwdMaxHolders || (mh + 1) * 512 > att) ctx->use_fwd = false;  // + the staged residual rows
         }
     }
     ctx->fwd_tm_host.resize(7 * m->n_layers + 1 + 12);
