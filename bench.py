@@ -297,6 +297,163 @@ def run_ours(args, rank, world):
     return out, host
 
 
+# ----------------------------------------------------------------------------- further workloads
+
+def _greedy_streams(v, loop, B, first_lens, steps):
+    """Run the plain greedy loop (one row per sequence and step) for `steps` steps, record each
+    sequence's committed tokens, then rewind every cache to its length before the run."""
+    import torch
+    from speculative_decoding_verify_02_gb300 import SDV_DRAFT_NONE
+    streams = [[int(t)] for t in loop.first.cpu().tolist()]
+    for _ in range(steps):
+        loop.step(drafter=SDV_DRAFT_NONE, ngram=False)
+        nc = loop.n_commit.cpu().numpy()
+        cm = loop.committed.cpu().numpy().reshape(B, loop.max_span)
+        for b in range(B):
+            streams[b] += cm[b, :nc[b]].tolist()
+    v.rewind_cache(torch.as_tensor(np.asarray(first_lens, dtype=np.int32)).cuda(), B)
+    torch.cuda.synchronize()
+    assert v.get_status() == 0
+    return streams
+
+
+def run_verify_workload(args, name, contexts, seed):
+    """Verify steps over B sequences whose drafts are the target's own greedy continuation with
+    each position replaced by a uniform token with probability 0.3 (mixed acceptance)."""
+    import torch
+    import synth
+    from synth import workloads
+    from speculative_decoding_verify_02_gb300 import SDV_DRAFT_TABLE, Verifier
+    from speculative_decoding_verify_02_gb300.runner import SpecLoop
+    shape = synth.QWEN3_4B if args.layers <= 0 else synth.QWEN3_4B.with_layers(args.layers)
+    t_setup = time.time()
+    host, dev = build_weights(shape, SEED)
+    B = len(contexts)
+    gen_steps = (args.warmup + args.steps) * (K_DRAFT + 1) + 16
+    max_ctx = max(len(c) for c in contexts) + gen_steps + 64
+    n_pages = sum(-(-(len(c) + gen_steps + 64) // 16) for c in contexts) + 8 * B
+    v = Verifier(shape, dev, page_size=16, n_pages=n_pages, max_batch=B, max_rows=128, max_span=128,
+                 max_context=max_ctx)
+    loop = SpecLoop(v, B=B, max_span=K_DRAFT + 1)
+    loop.prefill(contexts, chunk=128)
+    lens = [len(c) for c in contexts]
+    loop.start([10_000_000] * B, k_init=0)
+    streams = _greedy_streams(v, loop, B, lens, gen_steps)
+    table_len = gen_steps + 64
+    tables = np.stack([workloads.corrupt(seed, b, np.array((streams[b] + [0] * table_len)[:table_len]), 0.3,
+                                         shape.vocab) for b in range(B)]).astype(np.int32)
+    table = torch.as_tensor(tables.reshape(-1)).cuda()
+    loop.start([10_000_000] * B, k_init=K_DRAFT)
+    kw = dict(drafter=SDV_DRAFT_TABLE, table=table, table_stride=table_len, ngram=False)
+    loop.capture(**kw)
+    for _ in range(args.warmup):
+        loop.replay()
+    torch.cuda.synchronize()
+    setup_s = time.time() - t_setup
+    lens_t = torch.zeros(B, dtype=torch.int32, device="cuda")
+
+    def total_len():
+        v.cache_seq_len(lens_t)
+        torch.cuda.synchronize()
+        return int(lens_t.sum().item())
+
+    L0 = total_len()
+    clocks = ClockSampler(None)
+    clocks.start()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for _ in range(args.steps):
+        loop.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    committed = total_len() - L0
+    assert v.get_status() == 0
+    v.profile_enable(True)  # per-phase device time (events around each launch group, eager steps)
+    v.profile_read()
+    for _ in range(min(args.steps, 5)):
+        loop.step(**kw)
+    prof = v.profile_read()
+    v.profile_enable(False)
+    n_prof = min(args.steps, 5)
+    mean_ctx = (L0 + L0 + committed) / 2 / B
+    step_ms = ms / args.steps
+    S = K_DRAFT + 1
+    step_bytes = WEIGHT_BYTES_PER_STEP + B * (mean_ctx + S) * KV_BYTES_PER_TOKEN + B * S * EMBED_BYTES_PER_ROW
+    peak, peak_kind = peaks()
+    return {
+        "metric": f"committed tok/s (4B-shape verify, K=7, {name})",
+        "value": round(committed / (ms * 1e-3), 3), "unit": "tok/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "committed_per_step": round(committed / args.steps, 3),
+        "dtype": "bf16", "data": "synthetic (seeded random-init weights and tokens)",
+        "config": {"workload": name, "batch": B, "mean_context": round(mean_ctx, 1), "span": S,
+                   "drafts": "greedy continuation, each position uniform-replaced with p=0.3", "graph": True},
+        "verify_hbm_gbs": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
+        "step_roofline_frac": round(step_bytes / (step_ms * 1e-3) / 1e9 / peak, 4),
+        "step_bytes": int(step_bytes), "peak_kind": peak_kind, "clocks": clk, "setup_s": round(setup_s, 1),
+        "forward": os.environ.get("SDV_FORWARD", "layered"),
+        "phases_ms_per_step": {p: round(prof[p][0] / n_prof, 4) for p in prof},
+    }
+
+
+def run_ngram_workload(args):
+    """End-to-end n-gram speculation: 8 prompts of 1024 tokens (32-token spans, half repeating an
+    earlier span), 256 greedy tokens each, 2-gram prompt lookup with adaptive K (start 1, +2 on a
+    fully accepted round, -1 on any rejection, cap 7), against the same loop without drafts."""
+    import torch
+    import synth
+    from synth import workloads
+    from speculative_decoding_verify_02_gb300 import SDV_DRAFT_NGRAM, SDV_DRAFT_NONE, Verifier
+    from speculative_decoding_verify_02_gb300.runner import SpecLoop
+    shape = synth.QWEN3_4B
+    host, dev = build_weights(shape, SEED)
+    B, GEN = 8, 256
+    prompts = [workloads.span_repeat_prompt(5 + b, n_spans=32, span=32, vocab=shape.vocab) for b in range(B)]
+    out = {}
+    for mode in ("spec_off", "spec_on"):
+        v = Verifier(shape, dev, page_size=16, n_pages=B * ((1024 + GEN + 64) // 16 + 8), max_batch=B,
+                     max_rows=128, max_span=128, max_context=1024 + GEN + 64, ngram_capacity=1024 + GEN + 64)
+        loop = SpecLoop(v, B=B, max_span=8)
+        loop.prefill(prompts, chunk=128, ngram=(mode == "spec_on"))
+        loop.start([GEN] * B, k_init=1 if mode == "spec_on" else 0, adaptive=(mode == "spec_on"), k_max=7)
+        kw = dict(drafter=SDV_DRAFT_NGRAM if mode == "spec_on" else SDV_DRAFT_NONE, ngram=(mode == "spec_on"))
+        loop.capture(**kw)
+        torch.cuda.synchronize()
+        lens_t = torch.zeros(B, dtype=torch.int32, device="cuda")
+        v.cache_seq_len(lens_t)
+        torch.cuda.synchronize()
+        L0 = int(lens_t.sum().item())
+        s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        steps = 0
+        while True:  # blocks of 16 steps until every sequence has its 256 tokens
+            for _ in range(16):
+                loop.replay()
+            steps += 16
+            v.cache_seq_len(lens_t)
+            torch.cuda.synchronize()
+            if int(lens_t.sum().item()) - L0 >= B * (GEN - 1) or steps > 4 * GEN:
+                break
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        gen = int(lens_t.sum().item()) - L0 + B      # + the first token of each sequence (from prefill)
+        assert v.get_status() == 0
+        out[mode] = {"tok_s": round(gen / (ms * 1e-3), 2), "ms": round(ms, 2), "steps": steps, "tokens": gen}
+        del v, loop
+        torch.cuda.empty_cache()
+    return {"metric": "committed tok/s, n-gram spec on vs off (4B shape, b8, 1024-token repeat-heavy prompts, 256 tokens)",
+            "value": out["spec_on"]["tok_s"], "unit": "tok/s", "spec_off": out["spec_off"], "spec_on": out["spec_on"],
+            "speedup": round(out["spec_on"]["tok_s"] / out["spec_off"]["tok_s"], 3),
+            "note": "steps run in blocks of 16 between host checks; idle steps after the budget count in the time",
+            "forward": os.environ.get("SDV_FORWARD", "layered")}
+
+
 # ----------------------------------------------------------------------------- the oracle on the host cores
 
 def oracle_step_sample(host=None, n_layers_sample=1):
@@ -375,6 +532,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--workload", default="b1", choices=["b1", "b16", "ctx32k", "ngram"],
+                    help="b1 (default, the headline line): batch 1, 848-token context; b16: 16 sequences with "
+                         "contexts U[512, 4096]; ctx32k: batch 1, 32768-token context; ngram: end-to-end 2-gram "
+                         "speculation against the same loop without drafts")
     ap.add_argument("--layers", type=int, default=0,
                     help="decoder layers (default: all 36); fewer only for small profiling cases")
     args = ap.parse_args()
@@ -391,6 +552,22 @@ def main():
         return
 
     import torch
+    if args.workload != "b1":
+        if rank == 0:  # single-GPU measurement lines for the other workloads
+            import synth
+            from synth import workloads
+            vocab = synth.QWEN3_4B.vocab
+            if args.workload == "b16":
+                lens = workloads.context_lengths(3, 16)
+                ctxs = [workloads.uniform_context(3, int(n), vocab, name=f"b16.ctx.{b}") for b, n in enumerate(lens)]
+                out = run_verify_workload(args, "qwen3-4b-shape verify, batch 16, contexts U[512, 4096], K=7", ctxs, 3)
+            elif args.workload == "ctx32k":
+                ctxs = [workloads.uniform_context(4, 32768, vocab)]
+                out = run_verify_workload(args, "qwen3-4b-shape verify, batch 1, 32768-token context, K=7", ctxs, 4)
+            else:
+                out = run_ngram_workload(args)
+            print(json.dumps(out), flush=True)
+        return
     if world > 1:
         torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))

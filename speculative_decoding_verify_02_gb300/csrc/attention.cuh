@@ -39,6 +39,10 @@ struct AttnArgs {
     bf16 *out;               // [rows][nq*D] (hi plane), lo plane out_plane elements later
     size_t out_plane;        // 0: write the hi plane only (a plain bf16 output)
     int *status;
+    int splits;              // attention_group.cuh: CTAs sharing one group's chunks (1, 2, 4 or 8)
+    int p_lo;                // attention_group.cuh: 1 = probabilities as a hi/lo pair, 0 = bf16 only
+    int layer;               // attention_group.cuh: layer index in the pool tensor map
+    unsigned long long *trace;  // attention_group.cuh: optional [CTA][8] %globaltimer stamps, or nullptr
 };
 
 constexpr int kAttnThreads = 256;   // 8 warps: 4 query tiles x 2 key blocks

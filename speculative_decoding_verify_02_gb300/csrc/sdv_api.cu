@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "attention.cuh"
+#include "attention_group.cuh"
 #include "common.cuh"
 #include "fwd.cuh"
 #include "gemm.cuh"
@@ -115,6 +116,8 @@ struct sdv_ctx {
     float *attn_po = nullptr;
     float2 *attn_pml = nullptr;
     int *attn_cnt = nullptr;
+    int attn_splits = 1;
+    int attn_lo = 1;  // attention products with hi/lo pairs (SDV_ATTN_LO=0: bf16 only)
     // persistent forward
     bool use_fwd = true, fwd_coop = true;
     int *fwd_sync = nullptr, *fwd_done = nullptr, *fwd_tile_cnt = nullptr, *fwd_att_cnt = nullptr;
@@ -137,6 +140,8 @@ struct sdv_ctx {
     GemmPlan plan[5];         // qkv, o, gate/up, down, lm head
     std::vector<CUtensorMap> tm_wq, tm_wk, tm_wv, tm_wo, tm_wg, tm_wu, tm_wd;
     CUtensorMap tm_lm{};
+    CUtensorMap tm_kv{};     // the KV pool (encode_pool)
+    bool attn_tma = false;   // attention_group.cuh usable (page size a power of two in [8, 128])
     CUtensorMap tm_xb[4]{}, tm_ao[4]{}, tm_h[4]{};
     bool use_pdl = true;
     int gen_adaptive = 0, gen_kmax = 1;  // adaptive-K settings from sdv_gen_init
@@ -262,7 +267,15 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     int *done_lm = reinterpret_cast<int *>(take(sizeof(int)));
     auto *keys = reinterpret_cast<unsigned long long *>(take(sizeof(unsigned long long) * kRowsCap));
     float2 *rope = reinterpret_cast<float2 *>(take(sizeof(float2) * static_cast<size_t>(c.max_context) * (D / 2)));
-    const size_t nslots = static_cast<size_t>(work_cap) * m.n_kv_heads * grp * qrows;
+    // attention: CTAs per (group, kv head), fixed by the configuration (a row's arithmetic must not
+    // depend on the span): the largest power of two <= 8 that keeps the grid within four CTAs per SM
+    // for a full batch at full context and at most 64 partials per (sequence, kv head)
+    const int max_groups = ceil_div(c.max_context, kAttnGroup);
+    int splits = 8;
+    while (splits > 1 && (static_cast<long long>(B) * max_groups * m.n_kv_heads * splits > 4LL * sm_count ||
+                          max_groups * splits > 64))
+        splits >>= 1;
+    const size_t nslots = static_cast<size_t>(work_cap) * splits * m.n_kv_heads * grp * qrows;
     float *apo = reinterpret_cast<float *>(take(sizeof(float) * nslots * D));
     float2 *apml = reinterpret_cast<float2 *>(take(sizeof(float2) * nslots));
     int *acnt = reinterpret_cast<int *>(take(sizeof(int) * static_cast<size_t>(B) * m.n_kv_heads * kAttnCluster));
@@ -310,6 +323,7 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
         ctx->attn_po = apo;
         ctx->attn_pml = apml;
         ctx->attn_cnt = acnt;
+        ctx->attn_splits = splits;
         ctx->fwd_sync = fsync;
         ctx->n_sync = n_sync;
         ctx->fwd_done = fsync;
@@ -379,6 +393,21 @@ bool encode_planes(CUtensorMap *tm, const void *ptr, uint64_t rows, uint64_t col
     cuuint32_t box[3] = {64, box_rows, 2};
     cuuint32_t es[3] = {1, 1, 1};
     return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The paged KV pool as a 5-D bf16 tensor [layer * n_pages][K|V][kv_head][slot][dim]; box = 64 dims x
+// page_size slots of one (page, K|V, head), 128-byte swizzle.
+bool encode_pool(CUtensorMap *tm, const void *pool, const sdv_model_cfg &m, const sdv_cache_cfg &c) {
+    EncodeTiledFn enc = get_encoder();
+    if (!enc) return false;
+    const uint64_t D = m.head_dim, P = c.page_size, H = m.n_kv_heads;
+    cuuint64_t dims[5] = {D, P, H, 2, static_cast<cuuint64_t>(m.n_layers) * c.n_pages};
+    cuuint64_t strides[4] = {D * 2, P * D * 2, H * P * D * 2, 2 * H * P * D * 2};
+    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(P), 1, 1, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(pool), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -554,16 +583,38 @@ int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *
     a.counters = ctx->attn_cnt;
     a.out = out;
     a.status = ctx->st.status;
-    const dim3 grid(ctx->work_cap * kAttnCluster, m.n_kv_heads);
-    for (int q0 = 0; q0 < max_span; q0 += ctx->qrows) {
+    a.splits = ctx->attn_splits;
+    a.layer = layer;
+    a.trace = ctx->fwd_trace;  // the timeline buffer of sdv_fwd_trace, when set
+    a.p_lo = ctx->attn_lo;
+    if (!ctx->attn_lo) a.q_plane = 0;  // queries as bf16 only
+    if (!ctx->attn_tma) {  // 8-CTA clusters per 1024-position group (attention.cuh)
+        const dim3 grid(ctx->work_cap * kAttnCluster, m.n_kv_heads);
+        a.splits = 1;
+        for (int q0 = 0; q0 < max_span; q0 += ctx->qrows) {
+            a.q0 = q0;
+            cudaError_t e;
+            if (m.head_dim == 128)
+                e = launch_cluster(ctx, attn_kernel<128>, grid, dim3(kAttnThreads), AttnShape<128>::SMEM, st,
+                                   kAttnCluster, a);
+            else
+                e = launch_cluster(ctx, attn_kernel<64>, grid, dim3(kAttnThreads), AttnShape<64>::SMEM, st,
+                                   kAttnCluster, a);
+            if (e != cudaSuccess) return SDV_ERR_CUDA;
+        }
+        return SDV_OK;
+    }
+    // `splits` CTAs per (1024-position group, kv head), chunks pipelined inside each, at most
+    // kGrpRows query rows per launch (attention_group.cuh)
+    const dim3 grid(ctx->work_cap * ctx->attn_splits, m.n_kv_heads);
+    a.qrows = std::max(1, kGrpRows / ctx->grp);
+    for (int q0 = 0; q0 < max_span; q0 += a.qrows) {
         a.q0 = q0;
         cudaError_t e;
         if (m.head_dim == 128)
-            e = launch_cluster(ctx, attn_kernel<128>, grid, dim3(kAttnThreads), AttnShape<128>::SMEM, st,
-                               kAttnCluster, a);
+            e = launch(ctx, attn_group_kernel<128>, grid, dim3(kGrpThreads), GrpShape<128>::SMEM, st, a, ctx->tm_kv);
         else
-            e = launch_cluster(ctx, attn_kernel<64>, grid, dim3(kAttnThreads), AttnShape<64>::SMEM, st,
-                               kAttnCluster, a);
+            e = launch(ctx, attn_group_kernel<64>, grid, dim3(kGrpThreads), GrpShape<64>::SMEM, st, a, ctx->tm_kv);
         if (e != cudaSuccess) return SDV_ERR_CUDA;
     }
     return SDV_OK;
@@ -796,6 +847,8 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
         ok &= encode_2d(&ctx->tm_wd[l], L.w_down, H, F, 128);
     }
     ok &= encode_2d(&ctx->tm_lm, w->lm_head, m->vocab, H, 128);
+    ctx->attn_tma = c->page_size >= 8 && c->page_size <= kAttnChunk && (c->page_size & (c->page_size - 1)) == 0;
+    if (ctx->attn_tma) ok &= encode_pool(&ctx->tm_kv, d_kv_pool, *m, *c);
     for (int i = 0; i < 4 && ok; ++i) {
         ok &= encode_planes(&ctx->tm_xb[i], ctx->xb, kRowsCap, H, kNs[i]);
         ok &= encode_planes(&ctx->tm_ao[i], ctx->attn_o, kRowsCap, qdim, kNs[i]);
@@ -813,6 +866,8 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
     if (e == cudaSuccess) e = set_gemm_smem<128>();
     if (e == cudaSuccess) e = set_smem(attn_kernel<128>, AttnShape<128>::SMEM);
     if (e == cudaSuccess) e = set_smem(attn_kernel<64>, AttnShape<64>::SMEM);
+    if (e == cudaSuccess) e = set_smem(attn_group_kernel<128>, GrpShape<128>::SMEM);
+    if (e == cudaSuccess) e = set_smem(attn_group_kernel<64>, GrpShape<64>::SMEM);
     if (e == cudaSuccess) e = D == 128 ? set_fwd_smem_d<128>() : set_fwd_smem_d<64>();
     if (e != cudaSuccess) {
         delete ctx;
@@ -834,6 +889,8 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
         const char *ev = std::getenv("SDV_FORWARD");
         if (!(ev && std::strcmp(ev, "persistent") == 0)) ctx->use_fwd = false;
         if (c->page_size & (c->page_size - 1)) ctx->use_fwd = false;  // page index by shift
+        const char *al = std::getenv("SDV_ATTN_LO");
+        if (al && al[0] == '0') ctx->attn_lo = 0;
         const char *rg = std::getenv("SDV_RING");
         if (rg) ctx->fwd_ring = std::max(0, std::atoi(rg));
         // the kernel's unit arithmetic is 32-bit, and a split tile's partials must fit its staging region
