@@ -239,19 +239,29 @@ int sdv_profile_enable(sdv_ctx *ctx, int on);
  * recorded group into h_ms[8] and h_count[8], and clear the record. */
 int sdv_profile_read(sdv_ctx *ctx, float *h_ms, int32_t *h_count);
 
-/* Timeline of the persistent forward. With d_buf non-null, every later
- * sdv_spec_forward on the persistent path writes, for each CTA c (one per
- * SM) and phase p (5 per layer: QKV, attention, O, gate/up, down; then the LM
- * head), eight %globaltimer stamps in nanoseconds at d_buf[(c * phases + p) * 8
- * + e]: e = 0 the phase's inputs were ready, 1 its last MMA was issued, 2 its
- * epilogue (or attention) work finished, 3 its last weight load was issued;
- * attention phases, first item: 4 K/V and Q landed, 5 softmax and P.V done,
- * 6 partial parked, 7 merge done; GEMM phases, first segment: 4 accumulator
- * ready, 5 partial parked, 6 partials of a split tile loaded for its
- * reduction. Entries of events that did not happen keep their old value. The
- * buffer (uint64, 8-byte aligned, at least sm_count * phases * 64 bytes, else
- * SDV_ERR_ARG) stays the caller's; d_buf = NULL stops tracing. The pages have
- * no counterpart of this call: it is instrumentation. */
+/* Device timeline, for profiling. With d_buf non-null, later calls write
+ * %globaltimer stamps (nanoseconds) into it; entries of events that did not
+ * happen keep their old value.
+ *   Persistent forward: for each CTA c (one per SM) and phase p (5 per layer:
+ *   QKV, attention, O, gate/up, down; then the LM head), 16 stamps at
+ *   d_buf[(c * phases + p) * 16 + e]: e = 0 the phase's inputs were ready,
+ *   1 its last MMA was issued, 2 its epilogue (or attention) work finished,
+ *   3 its last weight load was issued; attention phases, first item: 4 K/V and
+ *   Q landed, 5 softmax and P.V done, 6 partial parked, 7 merge done; GEMM
+ *   phases, first segment: 4 accumulator ready, 5 partial parked, 6 partials
+ *   of a split tile loaded for its reduction. Needs at least
+ *   sm_count * phases * 128 bytes, else SDV_ERR_ARG.
+ *   Per-projection path: region r of 2048 * 16 stamps, CTA c of the launch at
+ *   d_buf[(r * 2048 + c) * 16 + e]. Region 0: the attention kernel (e = 0
+ *   start, then its chunk and merge events). Region 1 + p: the last GEMM
+ *   launch of projection p (0 QKV, 1 O, 2 gate/up, 3 down, 4 LM head), written
+ *   when the buffer holds 6 regions (1,572,864 bytes) and the launch has at
+ *   most 2048 CTAs: e = 0 CTA start, 1 activations ready (after the wait on
+ *   the previous kernel), 2 first stage landed, 3 last MMA issued,
+ *   4 accumulator ready, 5 partial parked, 6 all partials of the tile parked,
+ *   7 rows finished, 8 CTA end.
+ * The buffer (uint64, 8-byte aligned) stays the caller's; d_buf = NULL stops
+ * tracing. The pages have no counterpart of this call: it is instrumentation. */
 int sdv_fwd_trace(sdv_ctx *ctx, void *d_buf, size_t bytes);
 
 /* Paged attention without any device allocation, for callers that cannot

@@ -31,7 +31,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "--shared", "-Xcompiler", "-fPIC",
-           "-cudart", "shared", "-I", os.path.join(ROOT, "include"), *SRC, "-o", tmp]
+           "-cudart", "shared", "-I", os.path.join(ROOT, "include"),
+           *os.environ.get("SDV_NVCC_EXTRA", "").split(), *SRC, "-o", tmp]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.run(cmd, check=True)

@@ -2,16 +2,17 @@
 // [layer*page][K|V][kv head][slot][dim], and one 128-key chunk of a kv head is, per page, a box of
 // (page size) rows x 64 dims per half of the head dimension, landing 128-byte swizzled.
 //
-// A (sequence, 1024-position key group, kv head) is served by `splits` CTAs, each owning
-// 8 / splits consecutive 128-key chunks of the group (the split is fixed per context, so a row's
-// arithmetic never depends on the span). A CTA walks its chunks in position order with the next
-// chunk's K/V copy in flight while the current chunk is computed (two shared-memory buffers), and
-// keeps an online softmax (running max m, sum l, unnormalised o) per query row. At most 32 query
-// rows (heads x span rows) per launch; warp w handles query tile w & 1 against the fixed 32-key
-// quarter w >> 1 of every chunk (all eight warps busy at verify widths); the four quarters merge in
-// shared memory at the end, in quarter order. When one CTA covers the whole key range it writes the
-// output; otherwise every CTA parks its partial and the last to arrive merges all partials in
-// position order, staging them in shared memory a block of rows at a time.
+// A (sequence, 1024-position key group, kv head) is served by one thread-block cluster of
+// `splits` CTAs, each owning 8 / splits consecutive 128-key chunks of the group (the split is fixed
+// per context, so a row's arithmetic never depends on the span). A CTA walks its chunks in position
+// order with the next chunks' K/V copies in flight while the current chunk is computed, and keeps
+// an online softmax (running max m, sum l, unnormalised o) per query row. At most 32 query rows
+// (heads x span rows) per launch; warp w handles query tile w & 1 against the fixed 32-key quarter
+// w >> 1 of every chunk (all eight warps busy at verify widths). The quarter states stay in shared
+// memory; after a cluster barrier each CTA merges a slice of the rows over all splits x 4 states of
+// the group, reading the other CTAs' shared memory, in position order. With one key group that is
+// the output; with several, each group's state is parked in global memory and the last CTA of each
+// split index to arrive merges its rows over the groups, in group order.
 //
 // Keys are cut by position only and a chunk that is fully masked for a row leaves that row's
 // state exactly unchanged (scale 1, nothing added), so a row's result does not depend on how many
@@ -24,6 +25,11 @@
 namespace sdv {
 
 constexpr int kGrpThreads = 256;
+constexpr int kMaxKvHeads = 16;
+// the KV pool's tensor maps, one per kv head (kernel parameter space)
+struct KvMaps {
+    CUtensorMap m[kMaxKvHeads];
+};
 constexpr int kGrpChunks = kAttnGroup / kAttnChunk;  // 8 chunks of 128 keys
 constexpr int kGrpRows = 32;                         // query rows (heads x span rows) per launch
 constexpr int kGrpQuarters = 4;                      // fixed key partition of a chunk
@@ -33,26 +39,34 @@ template <int D>
 struct GrpShape {
     static constexpr int ROW = D * 2;
     static constexpr int Q_BYTES = 2 * kGrpRows * ROW;       // hi rows 0..31, lo rows 32..63
-    static constexpr int HALF = kAttnChunk * 128;            // one 64-dim half of a chunk's K (or V)
     static constexpr int KV_BYTES = kAttnChunk * ROW;        // K (or V) of one chunk: D / 64 halves
     static constexpr int NBUF = 3;                           // chunks in flight + the one computed
     static constexpr int BUF_OFF = Q_BYTES;                  // buffers: [NBUF][K | V]
     static constexpr int ML_OFF = Q_BYTES + NBUF * 2 * KV_BYTES;
     static constexpr int SMEM = ML_OFF + 2 * kAttnRows * 8 + 1024;  // + alignment slack
     // after the loop the buffer region holds the four key quarters' fp32 partials [32][D]
-    static_assert(NBUF * 2 * KV_BYTES >= kGrpQuarters * kGrpRows * D * 4, "partials must fit in the buffer region");
+    // quarter states after the loop: fp32 rows of D + 8 (the stride keeps a warp's float2 stores of
+    // eight rows x four column pairs on distinct banks)
+    static constexpr int QO_LD = D + 8;
+    // quarter states [quarter][32 rows][QO_LD], then the CTA's merged state [32 rows][QO_LD]
+    static constexpr int RECV_OFF = kGrpQuarters * kGrpRows * QO_LD * 4;
+    static_assert(NBUF * 2 * KV_BYTES >= RECV_OFF + kGrpRows * QO_LD * 4, "states must fit in the buffer region");
     static_assert(2 * kAttnRows * 8 >= kGrpQuarters * kGrpRows * 8, "quarter statistics must fit");
 };
 
-// byte offset of 16-byte piece c of key row r in a K or V chunk buffer: 64-dim halves of 128
-// keys x 128 bytes each, 128-byte swizzled (the TMA layout)
-__device__ __forceinline__ uint32_t swz_kv(int r, int c) {
-    return static_cast<uint32_t>((c >> 3) * (kAttnChunk * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// A chunk buffer holds, per page of the chunk, the page's K box then its V box; a box is lines
+// (half * P + slot) of 128 bytes, 128-byte swizzled (the TMA layout). Byte offset of 16-byte piece
+// c of key r (kv = 0 K, 1 V), for page size P = 1 << lp (P >= 8) and head dimension D.
+template <int D>
+__device__ __forceinline__ uint32_t swz_kv(int r, int c, int kv, int lp) {
+    const int P = 1 << lp;
+    return static_cast<uint32_t>(((r >> lp) * 2 + kv) * (P * D * 2) + ((c >> 3) * P + (r & (P - 1))) * 128 +
+                                 (((c & 7) ^ (r & 7)) << 4));
 }
 
 template <int D>
 __global__ void __launch_bounds__(kGrpThreads, 1)
-    attn_group_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tkv) {
+    attn_group_kernel(const AttnArgs a, const __grid_constant__ KvMaps tkv) {
     using S = GrpShape<D>;
     constexpr int CH = D / 8;  // 16-byte chunks per row
     extern __shared__ uint8_t sm_raw[];
@@ -64,16 +78,23 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
 
     pdl_trigger();
     pdl_wait();
-    // optional timeline: 0 start, 1 Q and page ids in, 2 first chunk landed, 3 chunks done, 4 quarters
-    // merged, 5 partial parked, 6 parts merged, 7 end; merge: 8 statistics staged, 9 weights done
+    // optional timeline: 0 start, 1 Q and page ids in, 2 first chunk landed, 3 chunks done, 4 the
+    // CTA states of the cluster in place, 5 cluster merge done (output or parked group state),
+    // 8 merge across groups done (13 started, 14 and 15 thread 0's first element: maximum found,
+    // sums formed); 10 second chunk landed, 11 second chunk computed, 12 last chunk
+    // landed (when there are more than two)
     auto stamp = [&](int ev) {
         if (a.trace && threadIdx.x == 0)
-            a.trace[(static_cast<size_t>(blockIdx.y) * gridDim.x + blockIdx.x) * 16 + ev] = globaltimer();
+            a.trace[((static_cast<size_t>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * 16 + ev] =
+                globaltimer();
     };
     stamp(0);
-    const int w = blockIdx.x / a.splits, sp = blockIdx.x % a.splits, g = blockIdx.y;
-    if (w >= *a.n_work) return;
-    const int4 wi = a.work[w];
+    // grid (splits, kv heads, work items): the CTAs of one wave cover every kv head, so their K/V
+    // reads spread over whole pages of the pool
+    const int w = blockIdx.z, sp = blockIdx.x, g = blockIdx.y;
+    const int n_work = *a.n_work;
+    const int4 wi = a.work[w];  // w < work_cap: inside the list (both loads in flight together)
+    if (w >= n_work) return;    // the whole cluster shares w, so it leaves together
     const int b = wi.x & 0xffff, grp_idx = wi.x >> 16;
     const int L = wi.y, S_b = wi.z, row0 = wi.w;
     const int ni = max(0, min(S_b - a.q0, a.qrows));
@@ -86,10 +107,9 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     const int c_per = kGrpChunks / a.splits;
     const int c_lo = sp * c_per, c_hi = min(c_lo + c_per, n_ch_group);  // this CTA's chunks (may be none)
     const int n_ch = max(0, c_hi - c_lo);
-    const int n_parts = n_groups * a.splits;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const size_t head_stride = static_cast<size_t>(a.page_size) * D;
     const bool has_lo = a.q_plane != 0;
+    const int lp = 31 - __clz(a.page_size);  // page size: a power of two in [8, 128]
 
     // Q rows j = i_local * grp + hh (span row q0 + i_local, head g*grp + hh), both planes
     for (int e = tid; e < 2 * Mpad * CH; e += kGrpThreads) {
@@ -109,7 +129,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         mbar_init(&full[1], 1);
         mbar_init(&full[2], 1);
         fence_mbar_init();
-        prefetch_tensormap(&tkv);
+        prefetch_tensormap(&tkv.m[g]);
     }
     const int pg0 = g0 / a.page_size, npg = (g1 - 1) / a.page_size - pg0 + 1;
     for (int i = tid; i < npg; i += kGrpThreads) {
@@ -118,32 +138,32 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     }
     __syncthreads();
 
-    // one chunk's K and V: per page of the chunk, per 64-dim half, one box (thread 0 issues)
+    // one chunk's K and V: per page of the chunk one box (K and V rows of head g, both 64-dim
+    // halves); the lanes of warp 0 issue them after lane 0 has posted the byte count
     const int ppc = kAttnChunk / a.page_size;  // pages per chunk
     auto load_chunk = [&](int ch, int buf) {  // ch: this CTA's chunk index
-        if (tid != 0) return;
+        if (warp != 0) return;
         uint8_t *kb = sm + S::BUF_OFF + buf * 2 * S::KV_BYTES;
         const int k0 = g0 + (c_lo + ch) * kAttnChunk, k1 = min(k0 + kAttnChunk, g1);
         const int p_first = k0 / a.page_size - pg0, p_last = (k1 - 1) / a.page_size - pg0;
+        const int box_bytes = 2 * a.page_size * D * 2;  // one head's K and V rows of a page
         int bytes = 0;
-        for (int pi = p_first; pi <= p_last; ++pi) {
+        for (int pi = p_first + lane; pi <= p_last; pi += 32) {
             const int page = page_s[pi];
-            if (page >= 0 && page < a.n_pages) bytes += 2 * (D / 64) * a.page_size * 128;
+            if (page >= 0 && page < a.n_pages) bytes += box_bytes;
         }
-        mbar_arrive_expect_tx(&full[buf], static_cast<uint32_t>(bytes));
-        for (int pi = p_first; pi <= p_last; ++pi) {
+        bytes = __reduce_add_sync(0xffffffffu, bytes);
+        const uint64_t pol_kv = policy_evict_first();  // K/V are read once per step: keep L2 for the rest
+        if (lane == 0) mbar_arrive_expect_tx(&full[buf], static_cast<uint32_t>(bytes));
+        __syncwarp();
+        for (int pi = p_first + lane; pi <= p_last; pi += 32) {
             const int page = page_s[pi];
             if (page < 0 || page >= a.n_pages) {
                 set_status(a.status, SDV_ERR_CAPACITY);
                 continue;
             }
-            const int row = (pi - p_first) * a.page_size;
-            const int e = a.layer * a.n_pages + page;
-#pragma unroll
-            for (int kv = 0; kv < 2; ++kv)
-#pragma unroll
-                for (int h = 0; h < D / 64; ++h)
-                    tma_load_5d(kb + kv * S::KV_BYTES + h * S::HALF + row * 128, &tkv, &full[buf], h * 64, 0, g, kv, e);
+            tma_load_5d_hint(kb + (pi - p_first) * box_bytes, &tkv.m[g], &full[buf], 0, 0, 0, 0,
+                             a.layer * a.n_pages + page, pol_kv);
         }
     };
     __syncthreads();  // barriers initialised, page ids in place
@@ -170,12 +190,14 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         const int buf = ch % S::NBUF;
         if (!mbar_wait(&full[buf], (ch / S::NBUF) & 1)) set_status(a.status, SDV_ERR_DEVICE_TIMEOUT);
         if (ch == 0) stamp(2);
-        const uint32_t sK = smem_u32(sm + S::BUF_OFF + buf * 2 * S::KV_BYTES), sV = sK + S::KV_BYTES;
+        if (ch == 1) stamp(10);
+        if (ch == n_ch - 1 && ch > 1) stamp(12);
+        const uint32_t sKV = smem_u32(sm + S::BUF_OFF + buf * 2 * S::KV_BYTES);
         {   // keys past the group end read as zero V rows (the pool holds stale data there)
             const int kstart = g0 + (c_lo + ch) * kAttnChunk, nvalid = min(kAttnChunk, g1 - kstart);
             for (int e = tid; e < (kAttnChunk - nvalid) * CH; e += kGrpThreads) {
                 const int r = nvalid + e / CH, c = e % CH;
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sV + swz_kv(r, c)), "r"(0u) : "memory");
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sKV + swz_kv<D>(r, c, 1, lp)), "r"(0u) : "memory");
             }
         }
         __syncthreads();
@@ -199,7 +221,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
                     const int key = kq * kGrpQKeys + nt * 8 + (i >> 1) * 8 + (lane & 7);
                     const int c = ks * 2 + (i & 1);
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4(sK + swz_kv(key, c), b0, b1, b2, b3);
+                    ldsm_x4(sKV + swz_kv<D>(key, c, 0, lp), b0, b1, b2, b3);
                     mma_bf16_16816(s[nt], qh, b0, b1);
                     mma_bf16_16816(s[nt + 1], qh, b2, b3);
                     if (has_lo) {
@@ -261,7 +283,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
                     const int key = kq * kGrpQKeys + kk * 16 + (i & 1) * 8 + (lane & 7);
                     const int c = dn + (i >> 1);
                     uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(sV + swz_kv(key, c), b0, b1, b2, b3);
+                    ldsm_x4_t(sKV + swz_kv<D>(key, c, 1, lp), b0, b1, b2, b3);
                     mma_bf16_16816(o[dn], ph, b0, b1);
                     mma_bf16_16816(o[dn + 1], ph, b2, b3);
                     if (a.p_lo) {
@@ -277,64 +299,63 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
             l0 = l0 * sc0 + rs0;
             l1 = l1 * sc1 + rs1;
         }
+        if (ch == 1) stamp(11);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic accesses before the refill
         __syncthreads();  // buffer `buf` is free
         if (ch + S::NBUF < n_ch) load_chunk(ch + S::NBUF, buf);
     }
 
     stamp(3);
-    // the four quarters' states -> shared memory [quarter][row][D] (rows without keys stay (-inf, 0, 0)),
-    // merged per row in quarter order into quarter 0's slots
+    // the four quarters' states -> shared memory: per [quarter][row] a row of QO_LD floats holding
+    // the unnormalised o, then (m, l) at D, D + 1; quarters without keys keep (-inf, 0, 0)
     float *qo = reinterpret_cast<float *>(sm + S::BUF_OFF);
-    float2 *qml = reinterpret_cast<float2 *>(sm + S::ML_OFF);  // [quarter][kGrpRows]
     if (mt * 16 < Mpad) {
-        float *dst = qo + static_cast<size_t>(kq) * kGrpRows * D;
+        float *dst = qo + static_cast<size_t>(kq) * kGrpRows * S::QO_LD;
 #pragma unroll
         for (int dn = 0; dn < D / 8; ++dn) {
-            *reinterpret_cast<float2 *>(&dst[jr0 * D + dn * 8 + tq * 2]) = make_float2(o[dn][0], o[dn][1]);
-            *reinterpret_cast<float2 *>(&dst[jr1 * D + dn * 8 + tq * 2]) = make_float2(o[dn][2], o[dn][3]);
+            *reinterpret_cast<float2 *>(&dst[jr0 * S::QO_LD + dn * 8 + tq * 2]) = make_float2(o[dn][0], o[dn][1]);
+            *reinterpret_cast<float2 *>(&dst[jr1 * S::QO_LD + dn * 8 + tq * 2]) = make_float2(o[dn][2], o[dn][3]);
         }
         if (tq == 0) {
-            qml[kq * kGrpRows + jr0] = make_float2(m0, l0);
-            qml[kq * kGrpRows + jr1] = make_float2(m1, l1);
+            *reinterpret_cast<float2 *>(&dst[jr0 * S::QO_LD + D]) = make_float2(m0, l0);
+            *reinterpret_cast<float2 *>(&dst[jr1 * S::QO_LD + D]) = make_float2(m1, l1);
         }
     }
     __syncthreads();
-    __shared__ float qw_s[kGrpRows][kGrpQuarters];
-    __shared__ float2 mlf_s[kGrpRows];
-    for (int j = tid; j < Mpad; j += kGrpThreads) {  // per row: merged (m, l) and the quarters' weights
+    // the CTA's state: quarters merged per row in quarter order -> cs [row][QO_LD] (o, then m, l)
+    float *cs = qo + S::RECV_OFF / 4;
+    for (int e = tid; e < M * (D / 4 + 1); e += kGrpThreads) {
+        const int j = e / (D / 4 + 1), c4 = e % (D / 4 + 1);
+        float2 st[kGrpQuarters];
         float Mx = -INFINITY;
 #pragma unroll
-        for (int q = 0; q < kGrpQuarters; ++q) Mx = fmaxf(Mx, qml[q * kGrpRows + j].x);
-        float l = 0.f;
-#pragma unroll
-        for (int q = 0; q < kGrpQuarters; ++q) {
-            const float2 ml = qml[q * kGrpRows + j];
-            const float wq = ml.x == -INFINITY ? 0.f : exp2f(ml.x - Mx);
-            qw_s[j][q] = wq;
-            l += wq * ml.y;
+        for (int k = 0; k < kGrpQuarters; ++k) {
+            st[k] = *reinterpret_cast<const float2 *>(&qo[(k * kGrpRows + j) * S::QO_LD + D]);
+            Mx = fmaxf(Mx, st[k].x);
         }
-        mlf_s[j] = make_float2(Mx, l);
-    }
-    __syncthreads();
-    for (int e4 = tid; e4 < Mpad * D / 4; e4 += kGrpThreads) {
-        const int j = e4 / (D / 4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wq[kGrpQuarters];
 #pragma unroll
-        for (int q = 0; q < kGrpQuarters; ++q) {
-            const float wq = qw_s[j][q];
-            const float4 x = reinterpret_cast<const float4 *>(qo + static_cast<size_t>(q) * kGrpRows * D)[e4];
-            acc.x += wq * x.x;
-            acc.y += wq * x.y;
-            acc.z += wq * x.z;
-            acc.w += wq * x.w;
+        for (int k = 0; k < kGrpQuarters; ++k) wq[k] = st[k].x == -INFINITY ? 0.f : exp2f(st[k].x - Mx);
+        if (c4 == D / 4) {  // the row's (m, l)
+            float l = 0.f;
+#pragma unroll
+            for (int k = 0; k < kGrpQuarters; ++k) l += wq[k] * st[k].y;
+            *reinterpret_cast<float2 *>(&cs[j * S::QO_LD + D]) = make_float2(Mx, l);
+        } else {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kGrpQuarters; ++k) {
+                const float4 x = *reinterpret_cast<const float4 *>(&qo[(k * kGrpRows + j) * S::QO_LD + c4 * 4]);
+                acc.x += wq[k] * x.x;
+                acc.y += wq[k] * x.y;
+                acc.z += wq[k] * x.z;
+                acc.w += wq[k] * x.w;
+            }
+            *reinterpret_cast<float4 *>(&cs[j * S::QO_LD + c4 * 4]) = acc;
         }
-        reinterpret_cast<float4 *>(qo)[e4] = acc;
     }
-    __syncthreads();
+    cluster_sync();  // every CTA's state of the group in place
     stamp(4);
-    float *po_s = qo;  // [row][D] unnormalised o of this CTA's keys
-    float2 *ml_s = mlf_s;
 
     auto store = [&](int j, int d, float v) {
         const int r = row0 + a.q0 + j / a.grp, h = g * a.grp + j % a.grp;
@@ -343,103 +364,121 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         a.out[oi] = pr.hi;
         if (a.out_plane) a.out[oi + a.out_plane] = pr.lo;
     };
-    if (n_parts == 1) {
-        for (int e = tid; e < M * D; e += kGrpThreads) store(e / D, e % D, po_s[e] / ml_s[e / D].y);
-        stamp(7);
-        return;
-    }
-    // park this CTA's partial; the last of (b, g) to arrive merges every part in position order
+    // Cluster merge: CTA `sp` finishes rows [j0, j1) over the splits' states, in split (position)
+    // order, reading the other CTAs' shared memory. With one key group that is the output;
+    // otherwise the group's (o, m, l) is parked for the merge across groups.
+    const int per = (M + a.splits - 1) / a.splits;
+    const int j0 = min(M, sp * per), j1 = min(M, j0 + per);
+    const bool multi = n_groups > 1;
     const size_t rowsw = static_cast<size_t>(a.grp) * a.qrows;
-    const size_t slot = (static_cast<size_t>(w) * a.splits + sp) * a.nkv + g;
-    for (int e = tid; e < M * D; e += kGrpThreads) a.part_o[(slot * rowsw + e / D) * D + e % D] = po_s[e];
-    for (int j = tid; j < M; j += kGrpThreads) a.part_ml[slot * rowsw + j] = ml_s[j];
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        int *cnt = &a.counters[(b * a.nkv + g) * kAttnCluster];
-        const int last = atomicAdd(cnt, 1) == n_parts - 1;
-        if (last) *cnt = 0;
-        last_s = last;
-    }
-    __syncthreads();
-    stamp(5);
-    if (!last_s) return;
-    __threadfence();
-    // parts of (b, g) in position order: part p = (group wfirst + p / splits, split p % splits); the
-    // work items of one sequence are consecutive
-    const int wfirst = w - grp_idx;
-    auto part_slot = [&](int p) {
-        return (static_cast<size_t>(wfirst) * a.splits + p) * a.nkv + g;
-    };
-    // (m, l) of every part and row, staged; per row the max Mx, each part's weight exp2(m - Mx) and
-    // the denominator; then each thread owns four-column groups of the output and adds the parts'
-    // o in part order from registers, loads for a batch of parts in flight together
-    if (n_parts * kGrpRows * 12 + kGrpRows * 4 > S::NBUF * 2 * S::KV_BYTES) {  // (over ~340 parts)
-        if (tid == 0) set_status(a.status, SDV_ERR_UNSUPPORTED);
-        return;
-    }
-    float2 *sml = reinterpret_cast<float2 *>(sm + S::BUF_OFF);          // [part][kGrpRows]
-    float *swt = reinterpret_cast<float *>(sml + n_parts * kGrpRows);     // [part][kGrpRows]
-    float *sden = swt + n_parts * kGrpRows;                               // [kGrpRows]
-    for (int e = tid; e < n_parts * M; e += kGrpThreads) {
-        const int p = e / M, j = e - p * M;
-        sml[p * kGrpRows + j] = __ldcg(&a.part_ml[part_slot(p) * rowsw + j]);
-    }
-    __syncthreads();
-    stamp(8);
-    for (int j = tid; j < M; j += kGrpThreads) {
+    const size_t gslot = static_cast<size_t>(w) * a.nkv + g;  // this group's parked state (multi)
+    const uint32_t cs_l = smem_u32(cs);
+    for (int it = tid; it < (j1 - j0) * (D / 4); it += kGrpThreads) {
+        const int j = j0 + it / (D / 4), d = (it % (D / 4)) * 4;
+        float2 ml[kGrpChunks];
+        float4 x[kGrpChunks];
         float Mx = -INFINITY;
-        for (int p = 0; p < n_parts; ++p) Mx = fmaxf(Mx, sml[p * kGrpRows + j].x);
+#pragma unroll
+        for (int c = 0; c < kGrpChunks; ++c) {
+            if (c < a.splits) {
+                const uint32_t row = mapa_shared(cs_l, static_cast<uint32_t>(c)) + j * S::QO_LD * 4;
+                ml[c] = ld_dsmem_f2(row + D * 4);
+                x[c] = ld_dsmem_f4(row + d * 4);
+                Mx = fmaxf(Mx, ml[c].x);
+            }
+        }
         float den = 0.f;
-        for (int p = 0; p < n_parts; ++p) {
-            const float2 ml = sml[p * kGrpRows + j];
-            const float sc = ml.x == -INFINITY ? 0.f : exp2f(ml.x - Mx);
-            swt[p * kGrpRows + j] = sc;
-            den += sc * ml.y;
+        float4 n = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < kGrpChunks; ++c) {
+            if (c < a.splits) {
+                const float wq = ml[c].x == -INFINITY ? 0.f : exp2f(ml[c].x - Mx);
+                den += wq * ml[c].y;
+                n.x += wq * x[c].x;
+                n.y += wq * x[c].y;
+                n.z += wq * x[c].z;
+                n.w += wq * x[c].w;
+            }
         }
-        sden[j] = den;
+        if (!multi) {
+            store(j, d, n.x / den);
+            store(j, d + 1, n.y / den);
+            store(j, d + 2, n.z / den);
+            store(j, d + 3, n.w / den);
+        } else {
+            *reinterpret_cast<float4 *>(&a.part_o[(gslot * rowsw + j) * D + d]) = n;
+            if (d == 0) a.part_ml[gslot * rowsw + j] = make_float2(Mx, den);
+        }
     }
-    __syncthreads();
-    stamp(9);
-    constexpr int PB = 4;                                   // parts per batch
-    constexpr int PER = kGrpRows * (D / 4) / kGrpThreads;   // four-column groups per thread
-    float4 num[PER];
-#pragma unroll
-    for (int i = 0; i < PER; ++i) num[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int p0 = 0; p0 < n_parts; p0 += PB) {
-        float4 x[PER][PB];
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int e4 = tid + i * kGrpThreads, j = e4 / (D / 4), d = (e4 % (D / 4)) * 4;
-#pragma unroll
-            for (int k = 0; k < PB; ++k)
-                if (j < M && p0 + k < n_parts)
-                    x[i][k] = __ldcg(reinterpret_cast<const float4 *>(a.part_o + (part_slot(p0 + k) * rowsw + j) * D + d));
+    cluster_arrive();  // this CTA's reads of the other CTAs' shared memory are done
+    stamp(5);
+    if (multi) {
+        // the last of the key groups' CTAs with this split index merges rows [j0, j1) over the
+        // groups' parked states, in group order
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            int *cnt = &a.counters[(b * a.nkv + g) * kAttnCluster + sp];
+            const int last = atomicAdd(cnt, 1) == n_groups - 1;
+            if (last) *cnt = 0;
+            last_s = last;
         }
+        __syncthreads();
+        if (last_s) {
+            __threadfence();
+            stamp(13);
+            const int wfirst = w - grp_idx;  // the work items of one sequence are consecutive
+            for (int it = tid; it < (j1 - j0) * (D / 4); it += kGrpThreads) {
+                const int j = j0 + it / (D / 4), d = (it % (D / 4)) * 4;
+                constexpr int QB = 16;  // groups whose loads are in flight together
+                auto slot_of = [&](int q) { return (static_cast<size_t>(wfirst) + q) * a.nkv + g; };
+                float Mx = -INFINITY;
+                for (int q0 = 0; q0 < n_groups; q0 += QB) {
+                    float mq[QB];
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int j = (tid + i * kGrpThreads) / (D / 4);
+                    for (int k = 0; k < QB; ++k)
+                        mq[k] = q0 + k < n_groups ? __ldcg(&a.part_ml[slot_of(q0 + k) * rowsw + j]).x : -INFINITY;
 #pragma unroll
-            for (int k = 0; k < PB; ++k)
-                if (j < M && p0 + k < n_parts) {
-                    const float sc = swt[(p0 + k) * kGrpRows + j];
-                    num[i].x += sc * x[i][k].x;
-                    num[i].y += sc * x[i][k].y;
-                    num[i].z += sc * x[i][k].z;
-                    num[i].w += sc * x[i][k].w;
+                    for (int k = 0; k < QB; ++k) Mx = fmaxf(Mx, mq[k]);
                 }
+                if (it == 0) stamp(14);
+                float den = 0.f;
+                float4 n = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int q0 = 0; q0 < n_groups; q0 += QB) {
+                    float2 st[QB];
+                    float4 x[QB];
+#pragma unroll
+                    for (int k = 0; k < QB; ++k) {
+                        st[k] = make_float2(-INFINITY, 0.f);
+                        x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (q0 + k < n_groups) {
+                            const size_t sl = slot_of(q0 + k);
+                            st[k] = __ldcg(&a.part_ml[sl * rowsw + j]);
+                            x[k] = __ldcg(reinterpret_cast<const float4 *>(&a.part_o[(sl * rowsw + j) * D + d]));
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < QB; ++k) {
+                        if (q0 + k < n_groups) {  // group order
+                            const float wq = st[k].x == -INFINITY ? 0.f : exp2f(st[k].x - Mx);
+                            den += wq * st[k].y;
+                            n.x += wq * x[k].x;
+                            n.y += wq * x[k].y;
+                            n.z += wq * x[k].z;
+                            n.w += wq * x[k].w;
+                        }
+                    }
+                }
+                if (it == 0) stamp(15);
+                store(j, d, n.x / den);
+                store(j, d + 1, n.y / den);
+                store(j, d + 2, n.z / den);
+                store(j, d + 3, n.w / den);
+            }
+            stamp(8);
         }
     }
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-        const int e4 = tid + i * kGrpThreads, j = e4 / (D / 4), d = (e4 % (D / 4)) * 4;
-        if (j >= M) continue;
-        const float den = sden[j];
-        store(j, d, num[i].x / den);
-        store(j, d + 1, num[i].y / den);
-        store(j, d + 2, num[i].z / den);
-        store(j, d + 3, num[i].w / den);
-    }
+    cluster_wait();  // no CTA leaves while another may still read its shared memory
     stamp(6);
 }
 

@@ -58,7 +58,18 @@ struct GemmArgs {
     float *logits;
     int *argmax_out, *done_counter;
     int vocab;
+    unsigned long long *trace;         // optional timeline: 16 %globaltimer stamps per CTA, or nullptr
 };
+
+__device__ __forceinline__ void gemm_stamp(const GemmArgs &a, int ev) {
+    if (a.trace) a.trace[static_cast<size_t>(blockIdx.x) * 16 + ev] = globaltimer();
+}
+
+// Shared memory given to the stage ring of one GEMM CTA. 104 KB lets two CTAs share an SM (the
+// next kernel's CTAs then start streaming weights while this one finishes).
+#ifndef SDV_GEMM_STAGE_KB
+#define SDV_GEMM_STAGE_KB 104
+#endif
 
 template <int N>
 struct GemmShape {
@@ -67,8 +78,8 @@ struct GemmShape {
     static constexpr int B_PLANE = N * BK * 2;      // one of the hi / lo planes
     static constexpr int B_BYTES = 2 * B_PLANE;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES_RAW = (104 * 1024) / STAGE_BYTES;  // two CTAs per SM
-    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int STAGES_RAW = (SDV_GEMM_STAGE_KB * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 16 ? 16 : STAGES_RAW;
     // The hi and lo planes are adjacent in the B stage (N rows each), so one MMA of width 2N
     // covers both: hi product in accumulator columns [0, N), lo product in [N, 2N). One MMA per
     // 16-wide k step instead of two: the tensor core's cost is per instruction at these widths.
@@ -81,6 +92,7 @@ struct GemmShape {
 };
 
 constexpr int kGemmThreads = 192;
+constexpr int kMaxSplits = 8;  // K splits of a tile: one thread-block cluster (portable size)
 
 // ------------------------------------------------------------------ epilogues
 // One warp finishes one row at a time. Lane l holds features l, l+32, l+64 and
@@ -102,35 +114,87 @@ struct EpiLayer {
     const bf16 *g_next;           // residual: gain of the RMSNorm that consumes x
 };
 
-__device__ __forceinline__ void epi_qkv_row(const GemmArgs &a, const EpiLayer &el, float rstd, int tile, int r,
-                                            int lane, float (&x)[4]) {
-    const int D = a.D;
-    int section, fbase;  // 0 = q, 1 = k, 2 = v; first feature of the tile inside its section
+// What the QKV epilogue of one row reads besides the accumulator: its position, the RoPE
+// (cos, sin) pairs of the lane's features and, for K and V tiles, the page holding the position.
+// Loaded while the MMAs run, so the row's finish does not wait on global memory.
+struct QkvRow {
+    int pos, page;
+    float2 c0, c1;
+};
+
+__device__ __forceinline__ int qkv_section(const GemmArgs &a, int tile, int &fbase) {
     if (tile < a.q_tiles) {
-        section = 0;
         fbase = tile * 128;
-    } else if (tile < a.q_tiles + a.k_tiles) {
-        section = 1;
-        fbase = (tile - a.q_tiles) * 128;
-    } else {
-        section = 2;
-        fbase = (tile - a.q_tiles - a.k_tiles) * 128;
+        return 0;
     }
+    if (tile < a.q_tiles + a.k_tiles) {
+        fbase = (tile - a.q_tiles) * 128;
+        return 1;
+    }
+    fbase = (tile - a.q_tiles - a.k_tiles) * 128;
+    return 2;
+}
+
+__device__ __forceinline__ QkvRow qkv_row_load(const GemmArgs &a, int tile, int r, int lane) {
+    int fbase;
+    const int section = qkv_section(a, tile, fbase);
+    QkvRow q;
+    q.pos = a.row_pos[r];
+    q.page = -1;
+    q.c0 = q.c1 = make_float2(1.f, 0.f);
+    if (section < 2) {
+        const int p = q.pos < 0 ? 0 : (q.pos >= a.rope_rows ? a.rope_rows - 1 : q.pos);
+        if (a.D == 128) {
+            q.c0 = a.rope[static_cast<size_t>(p) * 64 + lane];
+            q.c1 = a.rope[static_cast<size_t>(p) * 64 + lane + 32];
+        } else {
+            q.c0 = a.rope[static_cast<size_t>(p) * 32 + lane];
+        }
+    }
+    if (section > 0) {
+        const int seq = a.row_seq[r], slot_idx = q.pos / a.page_size;
+        if (seq >= 0 && q.pos >= 0 && slot_idx < a.pages_per_seq)
+            q.page = a.page_table[static_cast<size_t>(seq) * a.pages_per_seq + slot_idx];
+    }
+    return q;
+}
+
+// head-norm gains of the lane's features (row-independent): D = 128 features l + 32i; D = 64
+// g[0], g[1] = dims l, l + 32 (both heads of the tile share them)
+__device__ __forceinline__ void qkv_gains(const GemmArgs &a, const EpiLayer &el, int tile, int lane, float (&g)[4]) {
+    int fbase;
+    const int section = qkv_section(a, tile, fbase);
+    const bf16 *gain = section == 0 ? el.q_gain : el.k_gain;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) g[i] = 1.f;
+    if (section < 2 && a.qk_norm) {
+        if (a.D == 128) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) g[i] = __bfloat162float(gain[lane + 32 * i]);
+        } else {
+            g[0] = __bfloat162float(gain[lane]);
+            g[1] = __bfloat162float(gain[lane + 32]);
+        }
+    }
+}
+
+__device__ __forceinline__ void epi_qkv_core(const GemmArgs &a, const EpiLayer &el, float rstd, int tile, int r,
+                                             int lane, float (&x)[4], const QkvRow &q, const float (&g)[4]) {
+    const int D = a.D;
+    int fbase;  // first feature of the tile inside its section (0 = q, 1 = k, 2 = v)
+    const int section = qkv_section(a, tile, fbase);
 #pragma unroll
     for (int i = 0; i < 4; ++i) x[i] *= rstd;
-    const int pos = a.row_pos[r];
+    const int pos = q.pos;
     if (section < 2) {
-        const bf16 *gain = section == 0 ? el.q_gain : el.k_gain;
-        const int p = pos < 0 ? 0 : (pos >= a.rope_rows ? a.rope_rows - 1 : pos);
         if (D == 128) {  // one head: dims l, l+32, l+64, l+96; pairs (l, l+64), (l+32, l+96)
             if (a.qk_norm) {
                 const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
                 const float sc = rsqrtf(ss / 128.f + a.eps);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) x[i] *= sc * __bfloat162float(gain[lane + 32 * i]);
+                for (int i = 0; i < 4; ++i) x[i] *= sc * g[i];
             }
-            const float2 c0 = a.rope[static_cast<size_t>(p) * 64 + lane];
-            const float2 c1 = a.rope[static_cast<size_t>(p) * 64 + lane + 32];
+            const float2 c0 = q.c0, c1 = q.c1;
             const float y0 = x[0] * c0.x - x[2] * c0.y, y2 = x[2] * c0.x + x[0] * c0.y;
             const float y1 = x[1] * c1.x - x[3] * c1.y, y3 = x[3] * c1.x + x[1] * c1.y;
             x[0] = y0; x[1] = y1; x[2] = y2; x[3] = y3;
@@ -138,10 +202,9 @@ __device__ __forceinline__ void epi_qkv_row(const GemmArgs &a, const EpiLayer &e
             if (a.qk_norm) {
                 const float sa = rsqrtf(warp_sum(x[0] * x[0] + x[1] * x[1]) / 64.f + a.eps);
                 const float sb = rsqrtf(warp_sum(x[2] * x[2] + x[3] * x[3]) / 64.f + a.eps);
-                const float g0 = __bfloat162float(gain[lane]), g1 = __bfloat162float(gain[lane + 32]);
-                x[0] *= sa * g0; x[1] *= sa * g1; x[2] *= sb * g0; x[3] *= sb * g1;
+                x[0] *= sa * g[0]; x[1] *= sa * g[1]; x[2] *= sb * g[0]; x[3] *= sb * g[1];
             }
-            const float2 c = a.rope[static_cast<size_t>(p) * 32 + lane];
+            const float2 c = q.c0;
             const float y0 = x[0] * c.x - x[1] * c.y, y1 = x[1] * c.x + x[0] * c.y;
             const float y2 = x[2] * c.x - x[3] * c.y, y3 = x[3] * c.x + x[2] * c.y;
             x[0] = y0; x[1] = y1; x[2] = y2; x[3] = y3;
@@ -158,10 +221,7 @@ __device__ __forceinline__ void epi_qkv_row(const GemmArgs &a, const EpiLayer &e
         }
         return;
     }
-    const int seq = a.row_seq[r], slot_idx = pos / a.page_size;
-    int page = -1;
-    if (seq >= 0 && pos >= 0 && slot_idx < a.pages_per_seq)
-        page = a.page_table[static_cast<size_t>(seq) * a.pages_per_seq + slot_idx];
+    const int page = q.page;
     if (page < 0 || page >= a.n_pages) {
         if (lane == 0) set_status(a.status, SDV_ERR_CAPACITY);
         return;
@@ -176,18 +236,26 @@ __device__ __forceinline__ void epi_qkv_row(const GemmArgs &a, const EpiLayer &e
     }
 }
 
-// xs: the row's 128 residual values already staged in shared memory, or nullptr to read them
-__device__ __forceinline__ void epi_resid_row(const GemmArgs &a, const EpiLayer &el, int tile, int r, int lane,
-                                              float (&x)[4], const float *xs = nullptr) {
+__device__ __forceinline__ void epi_qkv_row(const GemmArgs &a, const EpiLayer &el, float rstd, int tile, int r,
+                                            int lane, float (&x)[4]) {
+    float g[4];
+    qkv_gains(a, el, tile, lane, g);
+    epi_qkv_core(a, el, rstd, tile, r, lane, x, qkv_row_load(a, tile, r, lane), g);
+}
+
+// residual-add epilogue of one row: xr = the row's residual values of the lane's features,
+// gn = the next RMSNorm's gains of those features (0 past n_out)
+__device__ __forceinline__ void epi_resid_core(const GemmArgs &a, int tile, int r, int lane, const float (&x)[4],
+                                               const float (&xr)[4], const float (&gn)[4]) {
     float sq = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int F = tile * 128 + lane + 32 * i;
         if (F < a.n_out) {
             const size_t o = static_cast<size_t>(r) * a.hidden + F;
-            const float xn = (xs ? xs[lane + 32 * i] : __ldcg(&a.x[o])) + x[i];
+            const float xn = xr[i] + x[i];
             a.x[o] = xn;
-            const Bf16Pair pr = split_bf16(xn * __bfloat162float(el.g_next[F]));
+            const Bf16Pair pr = split_bf16(xn * gn[i]);
             a.xb[o] = pr.hi;
             a.xb[o + static_cast<size_t>(a.rows_cap) * a.hidden] = pr.lo;
             sq += xn * xn;
@@ -195,6 +263,36 @@ __device__ __forceinline__ void epi_resid_row(const GemmArgs &a, const EpiLayer 
     }
     sq = warp_sum(sq);
     if (lane == 0) a.ss_out[static_cast<size_t>(tile) * a.rows_cap + r] = sq;
+}
+
+__device__ __forceinline__ void resid_row_load(const GemmArgs &a, int tile, int r, int lane, float (&xr)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int F = tile * 128 + lane + 32 * i;
+        xr[i] = F < a.n_out ? __ldcg(&a.x[static_cast<size_t>(r) * a.hidden + F]) : 0.f;
+    }
+}
+
+__device__ __forceinline__ void resid_gains(const GemmArgs &a, const EpiLayer &el, int tile, int lane, float (&gn)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int F = tile * 128 + lane + 32 * i;
+        gn[i] = F < a.n_out ? __bfloat162float(el.g_next[F]) : 0.f;
+    }
+}
+
+// xs: the row's 128 residual values already staged in shared memory, or nullptr to read them
+__device__ __forceinline__ void epi_resid_row(const GemmArgs &a, const EpiLayer &el, int tile, int r, int lane,
+                                              float (&x)[4], const float *xs = nullptr) {
+    float xr[4], gn[4];
+    if (xs) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) xr[i] = xs[lane + 32 * i];
+    } else {
+        resid_row_load(a, tile, r, lane, xr);
+    }
+    resid_gains(a, el, tile, lane, gn);
+    epi_resid_core(a, tile, r, lane, x, xr, gn);
 }
 
 __device__ __forceinline__ void epi_swiglu_row(const GemmArgs &a, float rstd, int tile, int r, int lane,
@@ -319,6 +417,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     const bool clustered = a.splits > 1;
 
     if (threadIdx.x == 0) {
+        gemm_stamp(a, 0);
         for (int s = 0; s < S::STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
@@ -361,6 +460,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             const int ahead = min(nk, pre + a.l2_ahead);
             for (int i = pre; i < ahead; ++i) prefetch_a<KIND>(&tmA0, &tmA1, &tmA2, a, tile, (kb0 + i) * 64);
             pdl_wait();  // activations come from the previous kernel
+            gemm_stamp(a, 1);
             for (int i = 0; i < pre; ++i)
                 tma_load_3d(smem + i * S::STAGE_BYTES + S::A_BYTES, &tmB, &full_bar[i], (kb0 + i) * 64, 0, 0);
             for (int i = pre; i < nk; ++i) {
@@ -387,19 +487,27 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                     break;
                 }
                 tc_fence_after();
+                if (i == 0) gemm_stamp(a, 2);
                 const uint64_t ad = sw128_desc(smem_u32(smem + s * S::STAGE_BYTES));
                 const uint64_t bd = sw128_desc(smem_u32(smem + s * S::STAGE_BYTES + S::A_BYTES));  // hi rows, then lo
 #pragma unroll
                 for (int k = 0; k < 4; ++k) umma_bf16(tmem, ad + 2 * k, bd + 2 * k, S::IDESC2, (i > 0 || k > 0) ? 1u : 0u);
                 umma_commit(&empty_bar[s]);
             }
+            gemm_stamp(a, 3);
             umma_commit(&accum_bar);
         }
     }
 
-    int R = 0;
+    // ---------------- epilogue warps 0-3. Rows of the tile this CTA finishes: all R, or its share
+    // [s0, s1) of a split tile. Warp w takes rows s0 + w + 4j; the first kPreRows of them get
+    // their row data (residual, RoPE, page) loaded while the MMAs still run.
+    constexpr int kPreRows = 4;
+    int R = 0, s0 = 0, s1 = 0;
+    float pre_x[kPreRows][4];  // EPI_RESID: residual values of the lane's features
+    QkvRow pre_q[kPreRows];    // EPI_QKV
+    float gl[4];               // row-independent gains (QKV head norm, or the next RMSNorm)
     if (warp < 4) {
-        // ---------------- epilogue warps 0-3: rstd rows, then the accumulator into shared memory
         pdl_wait();
         R = *a.nrows;
         if (R > N) {
@@ -417,8 +525,31 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 es.rstd[r] = s;
             }
         }
+        s1 = R;
+        if (clustered) {
+            const int per = (R + a.splits - 1) / a.splits;
+            s0 = min(R, static_cast<int>(cluster_ctarank()) * per);
+            s1 = min(R, s0 + per);
+        }
+        const EpiLayer el{a.q_gain, a.k_gain, a.kv_layer, a.g_next};
+        if constexpr (KIND == EPI_RESID) {
+            resid_gains(a, el, tile, lane, gl);
+#pragma unroll
+            for (int j = 0; j < kPreRows; ++j) {
+                const int r = s0 + warp + 4 * j;
+                if (r < s1) resid_row_load(a, tile, r, lane, pre_x[j]);
+            }
+        } else if constexpr (KIND == EPI_QKV) {
+            qkv_gains(a, el, tile, lane, gl);
+#pragma unroll
+            for (int j = 0; j < kPreRows; ++j) {
+                const int r = s0 + warp + 4 * j;
+                if (r < s1) pre_q[j] = qkv_row_load(a, tile, r, lane);
+            }
+        }
         if (!mbar_wait(&accum_bar, 0)) set_status(a.status, SDV_ERR_DEVICE_TIMEOUT);
         tc_fence_after();
+        if (threadIdx.x == 0) gemm_stamp(a, 4);
         const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         const int f = threadIdx.x;
         float v[32];
@@ -430,33 +561,61 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         }
     }
     // every partial of the tile is parked in shared memory (of each CTA of the cluster)
+    if (threadIdx.x == 0) gemm_stamp(a, 5);
     if (clustered) cluster_sync();
     else if (warp < 4) named_bar_sync(1, 128);
+    if (threadIdx.x == 0) gemm_stamp(a, 6);
     if (warp < 4) {
-        int s0 = 0, s1 = R;
-        if (clustered) {
-            const int per = (R + a.splits - 1) / a.splits;
-            s0 = min(R, static_cast<int>(cluster_ctarank()) * per);
-            s1 = min(R, s0 + per);
-        }
+        const EpiLayer el{a.q_gain, a.k_gain, a.kv_layer, a.g_next};
         const uint32_t red_local = smem_u32(red);
-        for (int r = s0 + warp; r < s1; r += 4) {
-            float x[4];
-            if (clustered) {
+        // four rows per pass, their loads issued together
+        for (int p = 0; s0 + warp + 16 * p < s1; ++p) {
+            float x[4][4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) x[i] = 0.f;
-                for (int q = 0; q < a.splits; ++q) {  // fixed split order
-                    const uint32_t base = mapa_shared(red_local, static_cast<uint32_t>(q)) + r * 512 + lane * 4;
+            for (int u = 0; u < 4; ++u) {
+                const int r = s0 + warp + 16 * p + 4 * u;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) x[i] += ld_dsmem(base + 128 * i);
+                for (int i = 0; i < 4; ++i) x[u][i] = 0.f;
+                if (r < s1) {
+                    if (clustered) {
+#pragma unroll
+                        for (int q = 0; q < kMaxSplits; ++q) {  // fixed split order
+                            if (q < a.splits) {
+                                const uint32_t base =
+                                    mapa_shared(red_local, static_cast<uint32_t>(q)) + r * 512 + lane * 4;
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) x[u][i] += ld_dsmem(base + 128 * i);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) x[u][i] = red[r * 128 + lane + 32 * i];
+                    }
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) x[i] = red[r * 128 + lane + 32 * i];
             }
-            epi_row<KIND>(a, EpiLayer{a.q_gain, a.k_gain, a.kv_layer, a.g_next}, es, tile, r, lane, x);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int r = s0 + warp + 16 * p + 4 * u;
+                if (r < s1) {
+                    if constexpr (KIND == EPI_RESID) {
+                        if (p == 0) {
+                            epi_resid_core(a, tile, r, lane, x[u], pre_x[u], gl);
+                        } else {
+                            float xr[4];
+                            resid_row_load(a, tile, r, lane, xr);
+                            epi_resid_core(a, tile, r, lane, x[u], xr, gl);
+                        }
+                    } else if constexpr (KIND == EPI_QKV) {
+                        epi_qkv_core(a, el, es.rstd[r], tile, r, lane, x[u],
+                                     p == 0 ? pre_q[u] : qkv_row_load(a, tile, r, lane), gl);
+                    } else {
+                        epi_row<KIND>(a, el, es, tile, r, lane, x[u]);
+                    }
+                }
+            }
         }
     }
+    if (threadIdx.x == 0) gemm_stamp(a, 7);
     if (clustered) cluster_sync();  // no CTA leaves while its partial may still be read
     if constexpr (KIND == EPI_LMHEAD) {
         if (warp < 4) {
@@ -478,6 +637,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     }
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) gemm_stamp(a, 8);
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, S::TMEM_COLS);

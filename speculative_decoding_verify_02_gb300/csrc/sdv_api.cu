@@ -133,6 +133,7 @@ struct sdv_ctx {
     std::vector<int> fwd_hold_host;
     int fwd_ring = 0;                         // ring stages in use, 0 = all; SDV_RING overrides
     unsigned long long *fwd_trace = nullptr;  // caller's timeline buffer, or nullptr
+    size_t fwd_trace_words = 0;
     std::vector<CUtensorMap> fwd_tm_host;
     std::vector<FwdLayer> fwd_layers_host;
     int ss_tiles = 0, grp = 0, qrows = 0, work_cap = 0, pages_per_seq = 0, ng_slots = 0;
@@ -140,7 +141,7 @@ struct sdv_ctx {
     GemmPlan plan[5];         // qkv, o, gate/up, down, lm head
     std::vector<CUtensorMap> tm_wq, tm_wk, tm_wv, tm_wo, tm_wg, tm_wu, tm_wd;
     CUtensorMap tm_lm{};
-    CUtensorMap tm_kv{};     // the KV pool (encode_pool)
+    KvMaps tm_kv{};          // the KV pool, one map per kv head (encode_pool)
     bool attn_tma = false;   // attention_group.cuh usable (page size a power of two in [8, 128])
     CUtensorMap tm_xb[4]{}, tm_ao[4]{}, tm_h[4]{};
     bool use_pdl = true;
@@ -193,6 +194,10 @@ struct PhaseMark {
 namespace {
 
 enum { P_QKV = 0, P_O = 1, P_GU = 2, P_DOWN = 3, P_LM = 4 };
+constexpr int kPlans = 5;
+// Timeline buffer on the per-projection path: region 0 for the attention CTAs, region 1 + p for
+// the GEMM launches of plan p; each region holds 16 stamps for up to kTraceRegionCtas CTAs.
+constexpr int kTraceRegionCtas = 2048;
 
 // Carve the workspace. With ctx == nullptr only the size is computed.
 size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8_t *base, int sm_count) {
@@ -267,9 +272,9 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     int *done_lm = reinterpret_cast<int *>(take(sizeof(int)));
     auto *keys = reinterpret_cast<unsigned long long *>(take(sizeof(unsigned long long) * kRowsCap));
     float2 *rope = reinterpret_cast<float2 *>(take(sizeof(float2) * static_cast<size_t>(c.max_context) * (D / 2)));
-    // attention: CTAs per (group, kv head), fixed by the configuration (a row's arithmetic must not
-    // depend on the span): the largest power of two <= 8 that keeps the grid within four CTAs per SM
-    // for a full batch at full context and at most 64 partials per (sequence, kv head)
+    // attention: CTAs (one cluster) per (group, kv head), fixed by the configuration (a row's
+    // arithmetic must not depend on the span): the largest power of two <= 8 that keeps the grid
+    // within four CTAs per SM for a full batch at full context and groups x splits <= 64
     const int max_groups = ceil_div(c.max_context, kAttnGroup);
     int splits = 8;
     while (splits > 1 && (static_cast<long long>(B) * max_groups * m.n_kv_heads * splits > 4LL * sm_count ||
@@ -399,17 +404,27 @@ bool encode_planes(CUtensorMap *tm, const void *ptr, uint64_t rows, uint64_t col
 
 // The paged KV pool as a 5-D bf16 tensor [layer * n_pages][K|V][kv_head][slot][dim]; box = 64 dims x
 // page_size slots of one (page, K|V, head), 128-byte swizzle.
-bool encode_pool(CUtensorMap *tm, const void *pool, const sdv_model_cfg &m, const sdv_cache_cfg &c) {
+// One map per kv head over the pool [layer x page][K|V][kv head][slot][dim], dimensions
+// [64 dims][slot][64-dim half][K|V][layer x page]: one box = a page's K and V rows of that head,
+// both halves, landing as [K|V][half][slot] lines of 128 bytes, so that eight consecutive keys of
+// one half sit on eight consecutive swizzle lines (8 KB per box at page size 16, head dim 128).
+bool encode_pool(KvMaps *tm, const void *pool, const sdv_model_cfg &m, const sdv_cache_cfg &c) {
     EncodeTiledFn enc = get_encoder();
     if (!enc) return false;
     const uint64_t D = m.head_dim, P = c.page_size, H = m.n_kv_heads;
-    cuuint64_t dims[5] = {D, P, H, 2, static_cast<cuuint64_t>(m.n_layers) * c.n_pages};
-    cuuint64_t strides[4] = {D * 2, P * D * 2, H * P * D * 2, 2 * H * P * D * 2};
-    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(P), 1, 1, 1};
+    if (H > kMaxKvHeads) return false;
+    cuuint64_t dims[5] = {64, P, D / 64, 2, static_cast<cuuint64_t>(m.n_layers) * c.n_pages};
+    cuuint64_t strides[4] = {D * 2, 128, H * P * D * 2, 2 * H * P * D * 2};
+    cuuint32_t box[5] = {64, static_cast<cuuint32_t>(P), static_cast<cuuint32_t>(D / 64), 2, 1};
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(pool), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    for (uint64_t h = 0; h < H; ++h) {
+        const char *base = static_cast<const char *>(pool) + h * P * D * 2;
+        if (enc(&tm->m[h], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<char *>(base), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    return true;
 }
 
 // 2-D bf16 map over a row-major [rows][cols] matrix; box = 64 columns x box_rows rows, 128-byte swizzle.
@@ -554,6 +569,11 @@ GemmArgs base_args(const sdv_ctx *ctx, int kind, int pidx) {
     a.partial = ctx->part[pidx];
     a.counters = ctx->cnt[pidx];
     a.part_stride = p.tiles * 128;
+    // timeline of the per-projection path: launch kind pidx writes region pidx + 1
+    const size_t region = static_cast<size_t>(kTraceRegionCtas) * 16;
+    if (ctx->fwd_trace && ctx->fwd_trace_words >= region * (kPlans + 1) &&
+        static_cast<size_t>(p.tiles) * p.splits <= kTraceRegionCtas)
+        a.trace = ctx->fwd_trace + region * (pidx + 1);
     return a;
 }
 
@@ -585,7 +605,9 @@ int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *
     a.status = ctx->st.status;
     a.splits = ctx->attn_splits;
     a.layer = layer;
-    a.trace = ctx->fwd_trace;  // the timeline buffer of sdv_fwd_trace, when set
+    // the timeline buffer of sdv_fwd_trace, when set: 16 stamps per CTA in region 0
+    if (static_cast<size_t>(ctx->work_cap) * ctx->attn_splits * m.n_kv_heads <= kTraceRegionCtas)
+        a.trace = ctx->fwd_trace;
     a.p_lo = ctx->attn_lo;
     if (!ctx->attn_lo) a.q_plane = 0;  // queries as bf16 only
     if (!ctx->attn_tma) {  // 8-CTA clusters per 1024-position group (attention.cuh)
@@ -604,17 +626,19 @@ int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *
         }
         return SDV_OK;
     }
-    // `splits` CTAs per (1024-position group, kv head), chunks pipelined inside each, at most
-    // kGrpRows query rows per launch (attention_group.cuh)
-    const dim3 grid(ctx->work_cap * ctx->attn_splits, m.n_kv_heads);
+    // a cluster of `splits` CTAs per (1024-position group, kv head), chunks pipelined inside each,
+    // at most kGrpRows query rows per launch (attention_group.cuh)
+    const dim3 grid(ctx->attn_splits, m.n_kv_heads, ctx->work_cap);
     a.qrows = std::max(1, kGrpRows / ctx->grp);
     for (int q0 = 0; q0 < max_span; q0 += a.qrows) {
         a.q0 = q0;
         cudaError_t e;
         if (m.head_dim == 128)
-            e = launch(ctx, attn_group_kernel<128>, grid, dim3(kGrpThreads), GrpShape<128>::SMEM, st, a, ctx->tm_kv);
+            e = launch_cluster(ctx, attn_group_kernel<128>, grid, dim3(kGrpThreads), GrpShape<128>::SMEM, st,
+                               ctx->attn_splits, a, ctx->tm_kv);
         else
-            e = launch(ctx, attn_group_kernel<64>, grid, dim3(kGrpThreads), GrpShape<64>::SMEM, st, a, ctx->tm_kv);
+            e = launch_cluster(ctx, attn_group_kernel<64>, grid, dim3(kGrpThreads), GrpShape<64>::SMEM, st,
+                               ctx->attn_splits, a, ctx->tm_kv);
         if (e != cudaSuccess) return SDV_ERR_CUDA;
     }
     return SDV_OK;
@@ -847,7 +871,8 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
         ok &= encode_2d(&ctx->tm_wd[l], L.w_down, H, F, 128);
     }
     ok &= encode_2d(&ctx->tm_lm, w->lm_head, m->vocab, H, 128);
-    ctx->attn_tma = c->page_size >= 8 && c->page_size <= kAttnChunk && (c->page_size & (c->page_size - 1)) == 0;
+    ctx->attn_tma = c->page_size >= 8 && c->page_size <= kAttnChunk && (c->page_size & (c->page_size - 1)) == 0 &&
+                    m->n_kv_heads <= kMaxKvHeads;
     if (ctx->attn_tma) ok &= encode_pool(&ctx->tm_kv, d_kv_pool, *m, *c);
     for (int i = 0; i < 4 && ok; ++i) {
         ok &= encode_planes(&ctx->tm_xb[i], ctx->xb, kRowsCap, H, kNs[i]);
@@ -1231,6 +1256,7 @@ int sdv_fwd_trace(sdv_ctx *ctx, void *d_buf, size_t bytes) {
     const size_t need = static_cast<size_t>(ctx->sm_count) * (5 * ctx->m.n_layers + 1) * 16 * sizeof(unsigned long long);
     if (bytes < need || reinterpret_cast<uintptr_t>(d_buf) % 8) return SDV_ERR_ARG;
     ctx->fwd_trace = static_cast<unsigned long long *>(d_buf);
+    ctx->fwd_trace_words = bytes / sizeof(unsigned long long);
     return SDV_OK;
 }
 
