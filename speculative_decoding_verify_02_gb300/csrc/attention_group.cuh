@@ -428,40 +428,56 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
             __threadfence();
             stamp(13);
             const int wfirst = w - grp_idx;  // the work items of one sequence are consecutive
-            for (int it = tid; it < (j1 - j0) * (D / 4); it += kGrpThreads) {
-                const int j = j0 + it / (D / 4), d = (it % (D / 4)) * 4;
-                constexpr int QB = 16;  // groups whose loads are in flight together
-                auto slot_of = [&](int q) { return (static_cast<size_t>(wfirst) + q) * a.nkv + g; };
+            const int nr = j1 - j0;
+            auto slot_of = [&](int q) { return (static_cast<size_t>(wfirst) + q) * a.nkv + g; };
+            // the groups' (m, l) of the slice's rows -> shared memory (the quarter-state region, no
+            // longer read); per row the maximum, each group's weight and the denominator (a warp per
+            // row, lanes over groups, group order kept by the fixed shuffle tree); then each thread
+            // sums float4 columns over the groups with a batch of loads in flight
+            if (n_groups * nr * 12 + nr * 4 > S::RECV_OFF) {  // the host keeps contexts within this
+                if (tid == 0) set_status(a.status, SDV_ERR_UNSUPPORTED);
+            } else {
+            float2 *gml = reinterpret_cast<float2 *>(qo);                 // [group][nr]
+            float *gw = reinterpret_cast<float *>(gml + n_groups * nr);   // [group][nr]
+            float *gden = gw + n_groups * nr;                             // [nr]
+            for (int e = tid; e < n_groups * nr; e += kGrpThreads) {
+                const int q = e / nr, r = e - q * nr;
+                gml[e] = __ldcg(&a.part_ml[slot_of(q) * rowsw + j0 + r]);
+            }
+            __syncthreads();
+            for (int r = warp; r < nr; r += kGrpThreads / 32) {
                 float Mx = -INFINITY;
-                for (int q0 = 0; q0 < n_groups; q0 += QB) {
-                    float mq[QB];
+                for (int q = lane; q < n_groups; q += 32) Mx = fmaxf(Mx, gml[q * nr + r].x);
 #pragma unroll
-                    for (int k = 0; k < QB; ++k)
-                        mq[k] = q0 + k < n_groups ? __ldcg(&a.part_ml[slot_of(q0 + k) * rowsw + j]).x : -INFINITY;
-#pragma unroll
-                    for (int k = 0; k < QB; ++k) Mx = fmaxf(Mx, mq[k]);
-                }
-                if (it == 0) stamp(14);
+                for (int o2 = 16; o2 > 0; o2 >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o2));
                 float den = 0.f;
+                for (int q = lane; q < n_groups; q += 32) {
+                    const float2 st = gml[q * nr + r];
+                    const float wq = st.x == -INFINITY ? 0.f : exp2f(st.x - Mx);
+                    gw[q * nr + r] = wq;
+                    den += wq * st.y;
+                }
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o2);
+                if (lane == 0) gden[r] = den;
+            }
+            __syncthreads();
+            stamp(14);
+            for (int it = tid; it < nr * (D / 4); it += kGrpThreads) {
+                const int r = it / (D / 4), j = j0 + r, d = (it % (D / 4)) * 4;
+                constexpr int QB = 16;  // groups whose loads are in flight together
                 float4 n = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int q0 = 0; q0 < n_groups; q0 += QB) {
-                    float2 st[QB];
                     float4 x[QB];
 #pragma unroll
-                    for (int k = 0; k < QB; ++k) {
-                        st[k] = make_float2(-INFINITY, 0.f);
-                        x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (q0 + k < n_groups) {
-                            const size_t sl = slot_of(q0 + k);
-                            st[k] = __ldcg(&a.part_ml[sl * rowsw + j]);
-                            x[k] = __ldcg(reinterpret_cast<const float4 *>(&a.part_o[(sl * rowsw + j) * D + d]));
-                        }
-                    }
+                    for (int k = 0; k < QB; ++k)
+                        x[k] = q0 + k < n_groups
+                                   ? __ldcg(reinterpret_cast<const float4 *>(&a.part_o[(slot_of(q0 + k) * rowsw + j) * D + d]))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int k = 0; k < QB; ++k) {
                         if (q0 + k < n_groups) {  // group order
-                            const float wq = st[k].x == -INFINITY ? 0.f : exp2f(st[k].x - Mx);
-                            den += wq * st[k].y;
+                            const float wq = gw[(q0 + k) * nr + r];
                             n.x += wq * x[k].x;
                             n.y += wq * x[k].y;
                             n.z += wq * x[k].z;
@@ -470,10 +486,12 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
                     }
                 }
                 if (it == 0) stamp(15);
+                const float den = gden[r];
                 store(j, d, n.x / den);
                 store(j, d + 1, n.y / den);
                 store(j, d + 2, n.z / den);
                 store(j, d + 3, n.w / den);
+            }
             }
             stamp(8);
         }

@@ -4,9 +4,10 @@
 // The verify span has few rows (K+1 per sequence, <= 128 in all), so the weight
 // matrix is the tcgen05 A operand (M = 128 output features per tile, streamed
 // from HBM by TMA with 128-byte swizzle) and the activations are the B operand
-// (N = rows padded to 16/32/64/128, read from L2), held as a bf16 hi/lo pair
-// applied by two MMAs, so activations keep about 16 significant bits while
-// the weights stay exactly bf16. The accumulator sits in
+// (N = rows padded to 16/32/64/128, read from L2), held as a bf16 hi/lo pair:
+// the planes are adjacent rows of the B tile, so one MMA of width 2N per k step
+// covers both and the epilogue adds the halves. Activations keep about 16
+// significant bits while the weights stay exactly bf16. The accumulator sits in
 // TMEM. Warp roles: warp 4 issues TMA, warp 5 issues MMAs, warps 0-3 run the
 // epilogue from tcgen05.ld. When K is split, the splits of one tile form a
 // thread-block cluster: each CTA parks its fp32 partial in its own shared
@@ -304,7 +305,7 @@ __device__ __forceinline__ void epi_swiglu_row(const GemmArgs &a, float rstd, in
         if (F < a.n_out) {
             const float gt = x[i] * rstd, up = x[i + 2] * rstd;
             const size_t o = static_cast<size_t>(r) * a.n_out + F;
-            const Bf16Pair pr = split_bf16(gt / (1.f + __expf(-gt)) * up);
+            const Bf16Pair pr = split_bf16(__fdividef(gt, 1.f + __expf(-gt)) * up);
             a.h_out[o] = pr.hi;
             a.h_out[o + static_cast<size_t>(a.rows_cap) * a.n_out] = pr.lo;
         }

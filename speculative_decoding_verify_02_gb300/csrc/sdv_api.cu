@@ -871,8 +871,12 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
         ok &= encode_2d(&ctx->tm_wd[l], L.w_down, H, F, 128);
     }
     ok &= encode_2d(&ctx->tm_lm, w->lm_head, m->vocab, H, 128);
+    // the group kernel stages the merge across key groups in its quarter-state region
+    const int grp_stage = m->head_dim == 128 ? GrpShape<128>::RECV_OFF : GrpShape<64>::RECV_OFF;
     ctx->attn_tma = c->page_size >= 8 && c->page_size <= kAttnChunk && (c->page_size & (c->page_size - 1)) == 0 &&
-                    m->n_kv_heads <= kMaxKvHeads;
+                    m->n_kv_heads <= kMaxKvHeads &&
+                    static_cast<long long>(ceil_div(c->max_context, kAttnGroup)) * kGrpRows * 12 + kGrpRows * 4 <=
+                        grp_stage;
     if (ctx->attn_tma) ok &= encode_pool(&ctx->tm_kv, d_kv_pool, *m, *c);
     for (int i = 0; i < 4 && ok; ++i) {
         ok &= encode_planes(&ctx->tm_xb[i], ctx->xb, kRowsCap, H, kNs[i]);
