@@ -36,6 +36,14 @@ K_DRAFT = 7
 SEED = 2
 WEIGHT_BYTES_PER_STEP = 8_044_936_192      # 36 layers + LM head + final norm (bf16)
 KV_BYTES_PER_TOKEN = 147_456               # 2 (K,V) x 8 heads x 128 x 2 B x 36 layers
+# DRAM bytes (read + write) that ncu measured per launch of the weight-streaming GEMM on the
+# per-projection path, in a 2-layer case of the same shapes (every launch of two timed steps):
+# QKV, O, gate/up, down per layer, then the LM head.
+# A launch streams its own weights, so a 36-layer step is 36 layers of the first four plus one
+# LM head; divided by the 145 launches it is the per-launch traffic beside `achieved`.
+GEMM_TRAFFIC_MB = {"qkv": 31.6998, "o": 21.3698, "gate_up": 99.9877, "down": 50.5655, "lm_head": 778.2215}
+GEMM_TRAFFIC_PER_LAUNCH = (36 * (GEMM_TRAFFIC_MB["qkv"] + GEMM_TRAFFIC_MB["o"] + GEMM_TRAFFIC_MB["gate_up"] +
+                                 GEMM_TRAFFIC_MB["down"]) + GEMM_TRAFFIC_MB["lm_head"]) * 1e6 / 145
 EMBED_BYTES_PER_ROW = 2560 * 2
 
 
@@ -205,10 +213,13 @@ def run_ours(args, rank, world):
         e2e_committed += n
     e2e_s = time.perf_counter() - t0
 
-    # latency against S = 1..17 (the verify-cost sweep)
+    # latency against S = 1..17 (the verify-cost sweep), each S from the configured context: the
+    # cache is rewound to CONTEXT positions first (a position rewind, pages past it released)
     sweep = {}
     if args.sweep:
+        ctx_len = torch.full((1,), CONTEXT, dtype=torch.int32, device="cuda")
         for S in range(1, 18):
+            v.rewind_cache(ctx_len, 1)
             lp = SpecLoop(v, B=1, max_span=S)
             lp.first.copy_(loop.committed[:1])       # continue from the current token
             lp.start([budget], k_init=S - 1)
@@ -243,6 +254,7 @@ def run_ours(args, rank, world):
     step_bytes = WEIGHT_BYTES_PER_STEP + (mean_ctx + S) * KV_BYTES_PER_TOKEN + S * EMBED_BYTES_PER_ROW
     peak, peak_kind = peaks()
     fwd_ms, fwd_launches = prof.get("forward", (0.0, 0))
+    dom_traffic = None
     if fwd_launches:
         # dominant kernel: the persistent forward (every layer and the LM head in one launch);
         # algorithmic bytes per launch = weights + the K/V it reads and writes
@@ -258,6 +270,8 @@ def run_ours(args, rank, world):
         dom_bytes = WEIGHT_BYTES_PER_STEP * args.steps + S * 2560 * 2 * 5 * 36 * args.steps
         dom_name = "gemm_kernel (tcgen05 weight-streaming GEMM, all projections + LM head)"
         launches_per_step = 4 + 2 + 36 * (1 + 2 + 3)
+        if args.layers <= 0 and dom_launches == 145 * args.steps:
+            dom_traffic = round(GEMM_TRAFFIC_PER_LAUNCH / 1e9, 5)   # GB per launch, as `achieved` per second
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     step_ms = ms_max / args.steps
     out = {
@@ -281,7 +295,9 @@ def run_ours(args, rank, world):
         "verify_hbm_gbs": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
         "step_roofline_frac": round(step_bytes / (step_ms * 1e-3) / 1e9 / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": dom_traffic,
+                     "traffic_unit": "GB per launch (ncu dram read + write)",
+                     "algorithmic": round(dom_bytes / max(dom_launches, 1) / 1e9, 5),
                      "kernel": dom_name,
                      "peak_kind": f"{peak_kind} (burst copy; each launch timed alone)",
                      "launches": dom_launches, "avg_launch_us": round(dom_ms * 1e3 / max(dom_launches, 1), 2)},
@@ -291,6 +307,7 @@ def run_ours(args, rank, world):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "sweep_ms_per_step": sweep,
+        "sweep_context": CONTEXT if args.sweep else None,
         "setup_s": round(setup_s, 1),
         "context_end": ctx_end,
     }
