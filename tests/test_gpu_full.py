@@ -53,15 +53,19 @@ def test_full_model_verify_step_848():
           f"near-tie flips {flips}")
 
 
-def test_attention_32k_context():
-    """Paged attention of an 8-row span over a 32768-token cache (synthetic
-    K/V and q), every output against the oracle's attention on the same bf16
-    values."""
+@pytest.mark.parametrize("L,S", [(32768, 8), (1020, 8), (2040, 16)])
+def test_attention_32k_context(L, S):
+    """Paged attention of a span over a long cache (synthetic K/V and q), every
+    output against the oracle's attention on the same bf16 values. 32768 + 8:
+    33 key groups of 1024 positions. 1020 + 8 and 2040 + 16: the span straddles
+    a group boundary, so its first rows see no key of the last group (that
+    group's state is empty for them); 16 rows also take two launches of 32
+    query rows (4 heads per kv head)."""
     import torch
     import speculative_decoding_verify_02_gb300 as sdv
     shape = synth.Shape("attn-4b-heads", 1, 256, 32, 8, 128, 256, 256)     # the 4B model's heads
     weights = {n: torch.zeros(d, dtype=torch.bfloat16, device="cuda") for n, d in shape.tensor_shapes().items()}
-    L, S, P = 32768, 8, 16
+    P = 16
     n_pages = (L + S) // P + 2
     v = sdv.Verifier(shape, weights, page_size=P, n_pages=n_pages, max_batch=1, max_rows=128, max_span=16,
                      max_context=n_pages * P)
@@ -88,5 +92,5 @@ def test_attention_32k_context():
                                 1 / np.sqrt(D))
     got = out.float().cpu().numpy().reshape(S, nq, D)
     err = np.abs(got - ref).max()
-    print(f"32k attention: max |d| {err:.3e}")
+    print(f"attention over {L} + {S}: max |d| {err:.3e}")
     assert err <= 2e-2
