@@ -252,9 +252,13 @@ int sdv_profile_read(sdv_ctx *ctx, float *h_ms, int32_t *h_count);
  *   of a split tile loaded for its reduction. Needs at least
  *   sm_count * phases * 128 bytes, else SDV_ERR_ARG.
  *   Per-projection path: region r of 2048 * 16 stamps, CTA c of the launch at
- *   d_buf[(r * 2048 + c) * 16 + e]. Region 0: the attention kernel (e = 0
- *   start, then its chunk and merge events). Region 1 + p: the last GEMM
- *   launch of projection p (0 QKV, 1 O, 2 gate/up, 3 down, 4 LM head), written
+ *   d_buf[(r * 2048 + c) * 16 + e]. Region 0: the attention kernel, CTA c in
+ *   launch order: e = 0 start, 1 Q and page ids in, 2 first chunk landed,
+ *   3 chunks done, 4 the CTA states of its cluster in place, 5 cluster merge
+ *   done, 10 second chunk landed, 11 second chunk computed, 12 last chunk
+ *   landed; the CTA merging across key groups: 13 merge started, 14 group
+ *   weights staged, 15 first element summed, 8 merge done. Region 1 + p: the
+ *   last GEMM launch of projection p (0 QKV, 1 O, 2 gate/up, 3 down, 4 LM head), written
  *   when the buffer holds 6 regions (1,572,864 bytes) and the launch has at
  *   most 2048 CTAs: e = 0 CTA start, 1 activations ready (after the wait on
  *   the previous kernel), 2 first stage landed, 3 last MMA issued,

@@ -78,16 +78,8 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *tm, ui
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
-// 5-D tiled bulk copy global -> shared (the paged KV pool as [layer*page][K|V][kv_head][slot][dim]).
-__device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1, int c2,
-                                            int c3, int c4) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, "
-        "%7}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-        : "memory");
-}
-// Same as tma_load_5d, with an L2 eviction-priority hint (createpolicy result).
+// 5-D tiled bulk copy global -> shared with an L2 eviction-priority hint (createpolicy result):
+// the paged KV pool, one map per kv head.
 __device__ __forceinline__ void tma_load_5d_hint(void *dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1,
                                                  int c2, int c3, int c4, uint64_t policy) {
     asm volatile(
@@ -259,16 +251,6 @@ __device__ __forceinline__ float ld_dsmem(uint32_t addr) {
     return v;
 }
 // Every thread of every CTA in the cluster must reach this (warp-converged).
-// bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from this CTA's shared
-// memory to a shared::cluster address, completing on the mbarrier at shared::cluster `bar`
-__device__ __forceinline__ void bulk_push(uint32_t dst_cluster, const void *src, uint32_t bytes,
-                                          uint32_t bar_cluster) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst_cluster),
-        "r"(smem_u32(src)), "r"(bytes), "r"(bar_cluster)
-        : "memory");
-}
 __device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
     float2 v;
     asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
