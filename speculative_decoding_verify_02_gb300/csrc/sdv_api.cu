@@ -117,7 +117,7 @@ struct sdv_ctx {
     float2 *attn_pml = nullptr;
     int *attn_cnt = nullptr;
     int attn_splits = 1;
-    int attn_lo = 1;  // attention products with hi/lo pairs (SDV_ATTN_LO=0: bf16 only)
+    int attn_lo = 1;  // attention products with hi/lo pairs (queries and probabilities)
     // persistent forward
     bool use_fwd = true, fwd_coop = true;
     int *fwd_sync = nullptr, *fwd_done = nullptr, *fwd_tile_cnt = nullptr, *fwd_att_cnt = nullptr;
@@ -131,7 +131,7 @@ struct sdv_ctx {
     int *fwd_hold = nullptr;         // device table of split-tile holders (FwdParams::hold)
     int fwd_hold_base[5] = {0, 0, 0, 0, 0};
     std::vector<int> fwd_hold_host;
-    int fwd_ring = 0;                         // ring stages in use, 0 = all; SDV_RING overrides
+    int fwd_ring = 0;                         // ring stages in use, 0 = all
     unsigned long long *fwd_trace = nullptr;  // caller's timeline buffer, or nullptr
     size_t fwd_trace_words = 0;
     std::vector<CUtensorMap> fwd_tm_host;
@@ -918,10 +918,6 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
         const char *ev = std::getenv("SDV_FORWARD");
         if (!(ev && std::strcmp(ev, "persistent") == 0)) ctx->use_fwd = false;
         if (c->page_size & (c->page_size - 1)) ctx->use_fwd = false;  // page index by shift
-        const char *al = std::getenv("SDV_ATTN_LO");
-        if (al && al[0] == '0') ctx->attn_lo = 0;
-        const char *rg = std::getenv("SDV_RING");
-        if (rg) ctx->fwd_ring = std::max(0, std::atoi(rg));
         // the kernel's unit arithmetic is 32-bit, and a split tile's partials must fit its staging region
         const int att = D == 128 ? FwdShape<128, 128>::STAGE_BYTES : FwdShape<128, 64>::STAGE_BYTES;
         for (int i = 0; i < 5; ++i) {
