@@ -59,6 +59,19 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def aggregate_replicas(committed, ms, e2e_committed, e2e_s, device):
+    """Whole-job totals over independent replicas (one per rank, no exchange on the data path):
+    committed tokens summed over the ranks, times the maximum over the ranks (the job ends with its
+    slowest replica). Returns (committed, ms, e2e committed, e2e seconds)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([committed, ms, e2e_committed, e2e_s], dtype=torch.float64, device=device)
+    tot, mx = t.clone(), t.clone()
+    dist.all_reduce(tot, op=dist.ReduceOp.SUM)
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    return float(tot[0]), float(mx[1]), float(tot[2]), float(mx[3])
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle sampling during the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -238,14 +251,8 @@ def run_ours(args, rank, world):
 
     # aggregate over ranks: tokens summed, time = max
     if world > 1:
-        t = torch.tensor([committed, ms, e2e_committed, e2e_s], dtype=torch.float64, device="cuda")
-        tot = t.clone()
-        torch.distributed.all_reduce(tot[0:1], op=torch.distributed.ReduceOp.SUM)
-        torch.distributed.all_reduce(tot[2:3], op=torch.distributed.ReduceOp.SUM)
-        mx = t.clone()
-        torch.distributed.all_reduce(mx, op=torch.distributed.ReduceOp.MAX)
-        committed_all, ms_max = float(tot[0]), float(mx[1])
-        e2e_committed_all, e2e_max = float(tot[2]), float(mx[3])
+        committed_all, ms_max, e2e_committed_all, e2e_max = aggregate_replicas(committed, ms, e2e_committed, e2e_s,
+                                                                               "cuda")
     else:
         committed_all, ms_max, e2e_committed_all, e2e_max = committed, ms, e2e_committed, e2e_s
 
