@@ -53,14 +53,15 @@ def test_full_model_verify_step_848():
           f"near-tie flips {flips}")
 
 
-@pytest.mark.parametrize("L,S", [(32768, 8), (1020, 8), (2040, 16)])
-def test_attention_32k_context(L, S):
-    """Paged attention of a span over a long cache (synthetic K/V and q), every
-    output against the oracle's attention on the same bf16 values. 32768 + 8:
-    33 key groups of 1024 positions. 1020 + 8 and 2040 + 16: the span straddles
-    a group boundary, so its first rows see no key of the last group (that
-    group's state is empty for them); 16 rows also take two launches of 32
-    query rows (4 heads per kv head)."""
+def test_attention_32k_context():
+    """Paged attention of an 8-row span over a 32768-token cache (33 key groups
+    of 1024 positions)."""
+    attention_long_context(32768, 8)
+
+
+def attention_long_context(L, S):
+    """Paged attention of an S-row span over an L-token cache (synthetic K/V and
+    q), every output against the oracle's attention on the same bf16 values."""
     import torch
     import speculative_decoding_verify_02_gb300 as sdv
     shape = synth.Shape("attn-4b-heads", 1, 256, 32, 8, 128, 256, 256)     # the 4B model's heads
