@@ -260,25 +260,16 @@ def run_ours(args, rank, world):
     S = K_DRAFT + 1
     step_bytes = WEIGHT_BYTES_PER_STEP + (mean_ctx + S) * KV_BYTES_PER_TOKEN + S * EMBED_BYTES_PER_ROW
     peak, peak_kind = peaks()
-    fwd_ms, fwd_launches = prof.get("forward", (0.0, 0))
+    # dominant kernel: the weight-streaming GEMM (every projection and the LM head)
+    gemm_phases = ("qkv_gemm", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm")
+    dom_ms = sum(prof[p][0] for p in gemm_phases)
+    dom_launches = sum(prof[p][1] for p in gemm_phases)
+    dom_bytes = WEIGHT_BYTES_PER_STEP * args.steps + S * 2560 * 2 * 5 * 36 * args.steps
+    dom_name = "gemm_kernel (tcgen05 weight-streaming GEMM, all projections + LM head)"
+    launches_per_step = 4 + 2 + 36 * (1 + 2 + 3)
     dom_traffic = None
-    if fwd_launches:
-        # dominant kernel: the persistent forward (every layer and the LM head in one launch);
-        # algorithmic bytes per launch = weights + the K/V it reads and writes
-        dom_ms, dom_launches = fwd_ms, fwd_launches
-        dom_bytes = (WEIGHT_BYTES_PER_STEP + (prof_ctx + S) * KV_BYTES_PER_TOKEN) * fwd_launches
-        dom_name = "fwd_kernel (persistent forward: 36 layers + LM head, tcgen05 weight streaming)"
-        launches_per_step = 6                     # propose, ensure, prepare, forward, accept, rewind
-    else:
-        # dominant kernel: the weight-streaming GEMM (every projection and the LM head)
-        gemm_phases = ("qkv_gemm", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm")
-        dom_ms = sum(prof[p][0] for p in gemm_phases)
-        dom_launches = sum(prof[p][1] for p in gemm_phases)
-        dom_bytes = WEIGHT_BYTES_PER_STEP * args.steps + S * 2560 * 2 * 5 * 36 * args.steps
-        dom_name = "gemm_kernel (tcgen05 weight-streaming GEMM, all projections + LM head)"
-        launches_per_step = 4 + 2 + 36 * (1 + 2 + 3)
-        if args.layers <= 0 and dom_launches == 145 * args.steps:
-            dom_traffic = round(GEMM_TRAFFIC_PER_LAUNCH / 1e9, 5)   # GB per launch, as `achieved` per second
+    if args.layers <= 0 and dom_launches == 145 * args.steps:
+        dom_traffic = round(GEMM_TRAFFIC_PER_LAUNCH / 1e9, 5)   # GB per launch, as `achieved` per second
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     step_ms = ms_max / args.steps
     out = {
@@ -419,7 +410,6 @@ def run_verify_workload(args, name, contexts, seed):
         "verify_hbm_gbs": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
         "step_roofline_frac": round(step_bytes / (step_ms * 1e-3) / 1e9 / peak, 4),
         "step_bytes": int(step_bytes), "peak_kind": peak_kind, "clocks": clk, "setup_s": round(setup_s, 1),
-        "forward": os.environ.get("SDV_FORWARD", "layered"),
         "phases_ms_per_step": {p: round(prof[p][0] / n_prof, 4) for p in prof},
     }
 
@@ -474,8 +464,7 @@ def run_ngram_workload(args):
     return {"metric": "committed tok/s, n-gram spec on vs off (4B shape, b8, 1024-token repeat-heavy prompts, 256 tokens)",
             "value": out["spec_on"]["tok_s"], "unit": "tok/s", "spec_off": out["spec_off"], "spec_on": out["spec_on"],
             "speedup": round(out["spec_on"]["tok_s"] / out["spec_off"]["tok_s"], 3),
-            "note": "steps run in blocks of 16 between host checks; idle steps after the budget count in the time",
-            "forward": os.environ.get("SDV_FORWARD", "layered")}
+            "note": "steps run in blocks of 16 between host checks; idle steps after the budget count in the time"}
 
 
 # ----------------------------------------------------------------------------- the oracle on the host cores

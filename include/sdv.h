@@ -235,41 +235,36 @@ int sdv_op_attention(sdv_ctx *ctx, int layer, const void *d_q, const int32_t *d_
  * records CUDA events around each launch group on its stream; this removes
  * the launch overlap between kernels, so durations are those of each kernel
  * run on its own. Groups: 0 prepare/embed, 1 QKV GEMM, 2 attention, 3 O GEMM,
- * 4 gate/up GEMM, 5 down GEMM, 6 LM-head GEMM (launch-per-projection path),
- * 7 the persistent forward (every layer and the LM head in one launch). */
+ * 4 gate/up GEMM, 5 down GEMM, 6 LM-head GEMM. */
 int sdv_profile_enable(sdv_ctx *ctx, int on);
 
 /* Synchronise, add the elapsed milliseconds and launch counts of every
- * recorded group into h_ms[8] and h_count[8], and clear the record. */
+ * recorded group into h_ms[7] and h_count[7], and clear the record. */
 int sdv_profile_read(sdv_ctx *ctx, float *h_ms, int32_t *h_count);
 
-/* Device timeline, for profiling. With d_buf non-null, later calls write
- * %globaltimer stamps (nanoseconds) into it; entries of events that did not
- * happen keep their old value.
- *   Persistent forward: for each CTA c (one per SM) and phase p (5 per layer:
- *   QKV, attention, O, gate/up, down; then the LM head), 16 stamps at
- *   d_buf[(c * phases + p) * 16 + e]: e = 0 the phase's inputs were ready,
- *   1 its last MMA was issued, 2 its epilogue (or attention) work finished,
- *   3 its last weight load was issued; attention phases, first item: 4 K/V and
- *   Q landed, 5 softmax and P.V done, 6 partial parked, 7 merge done; GEMM
- *   phases, first segment: 4 accumulator ready, 5 partial parked, 6 partials
- *   of a split tile loaded for its reduction. Needs at least
- *   sm_count * phases * 128 bytes, else SDV_ERR_ARG.
- *   Per-projection path: region r of 2048 * 16 stamps, CTA c of the launch at
- *   d_buf[(r * 2048 + c) * 16 + e]. Region 0: the attention kernel, CTA c in
- *   launch order: e = 0 start, 1 Q and page ids in, 2 first chunk landed,
- *   3 chunks done, 4 the CTA states of its cluster in place, 5 cluster merge
- *   done, 10 second chunk landed, 11 second chunk computed, 12 last chunk
- *   landed; the CTA merging across key groups: 13 merge started, 14 group
- *   weights staged, 15 first element summed, 8 merge done. Region 1 + p: the
- *   last GEMM launch of projection p (0 QKV, 1 O, 2 gate/up, 3 down, 4 LM head), written
- *   when the buffer holds 6 regions (1,572,864 bytes) and the launch has at
- *   most 2048 CTAs: e = 0 CTA start, 1 activations ready (after the wait on
+/* Device timeline, for profiling inside a captured or timed step without
+ * changing its launches. With d_buf non-null, later sdv_spec_forward calls
+ * write %globaltimer stamps (nanoseconds) into it; entries of events that did
+ * not happen keep their old value. The buffer is cut into regions of
+ * 2048 CTAs x 16 stamps (262,144 bytes), one per launch of a forward:
+ * layer l uses region 5l for its attention and 5l + 1 + p for its GEMM
+ * launches (p = 0 QKV, 1 O, 2 gate/up, 3 down); the LM head uses region
+ * 5 n_layers. CTA c of a launch writes d_buf[region * 32768 + c * 16 + e]; a
+ * launch with more than 2048 CTAs, or whose region lies past the buffer, is
+ * not traced.
+ *   GEMM launches: e = 0 CTA start, 1 activations ready (after the wait on
  *   the previous kernel), 2 first stage landed, 3 last MMA issued,
  *   4 accumulator ready, 5 partial parked, 6 all partials of the tile parked,
  *   7 rows finished, 8 CTA end.
- * The buffer (uint64, 8-byte aligned) stays the caller's; d_buf = NULL stops
- * tracing. The pages have no counterpart of this call: it is instrumentation. */
+ *   Attention (CTA in launch order): e = 0 start, 1 Q and page ids in, 2 first
+ *   chunk landed, 3 chunks done, 4 the CTA states of its cluster in place,
+ *   5 cluster merge done, 6 CTA end, 10 second chunk landed, 11 second chunk
+ *   computed, 12 last chunk landed; the CTA merging across key groups:
+ *   13 merge started, 14 group weights staged, 15 first element summed,
+ *   8 merge done.
+ * At least 5 regions (1,310,720 bytes), else SDV_ERR_ARG. The buffer
+ * (uint64, 8-byte aligned) stays the caller's; d_buf = NULL stops tracing.
+ * The pages have no counterpart of this call: it is instrumentation. */
 int sdv_fwd_trace(sdv_ctx *ctx, void *d_buf, size_t bytes);
 
 /* Paged attention without any device allocation, for callers that cannot

@@ -33,8 +33,9 @@ EXPORTS = (
     "sdv_op_attention", "sdv_profile_enable", "sdv_profile_read", "sdv_paged_attention_noalloc",
     "sdv_fwd_trace",
 )
-PHASES = ("prepare", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm",
-          "forward")
+PHASES = ("prepare", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm")
+# sdv_fwd_trace: stamps per CTA, CTAs per region (one region per launch of a forward)
+TRACE_STAMPS, TRACE_REGION_CTAS = 16, 2048
 
 
 class SdvError(RuntimeError):
@@ -255,8 +256,8 @@ class Verifier:
         return {PHASES[i]: (ms[i], cnt[i]) for i in range(len(PHASES))}
 
     def fwd_trace(self, buf):
-        """Record the persistent forward's per-CTA, per-phase timeline into `buf`
-        (a uint64 device tensor of sm_count x phases x 8), or stop with None."""
+        """Record the per-launch, per-CTA device timeline of later forwards into
+        `buf` (an int64 device tensor of regions x 2048 x 16), or stop with None."""
         n = buf.numel() * buf.element_size() if buf is not None else 0
         _check(lib().sdv_fwd_trace(self.ctx, _ptr(buf) if buf is not None else None, n), "fwd_trace")
 

@@ -90,6 +90,13 @@ struct GemmShape {
     static constexpr uint32_t IDESC2 = idesc_bf16(128, 2 * N);
     static_assert(STAGES >= 2, "pipeline too shallow");
     static_assert(B_PLANE % 1024 == 0, "B planes must keep 1024-byte alignment");
+    // one MMA covers both planes: 2N accumulator columns, a legal kind::f16 width for M = 128
+    static_assert(2 * N % 16 == 0 && 2 * N <= 256, "MMA width 2N must be a multiple of 16, at most 256");
+    static_assert(TMEM_COLS >= 2 * N && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation must hold 2N columns");
+    static_assert(2 * TMEM_COLS <= 512, "two co-resident CTAs must fit in the SM's 512 TMEM columns");
+    // the fp32 row tile [N][128] that the epilogue parks reuses the stage memory
+    static_assert(N * 128 * 4 <= STAGES * STAGE_BYTES, "parked row tile must fit in the stage ring");
+    static_assert(2 * (SMEM_BYTES + 1024) <= 227 * 1024, "two CTAs per SM must fit in shared memory");
 };
 
 constexpr int kGemmThreads = 192;
@@ -464,11 +471,14 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             gemm_stamp(a, 1);
             for (int i = 0; i < pre; ++i)
                 tma_load_3d(smem + i * S::STAGE_BYTES + S::A_BYTES, &tmB, &full_bar[i], (kb0 + i) * 64, 0, 0);
+            int issued = pre;
+            bool timed_out = false;
             for (int i = pre; i < nk; ++i) {
                 const int s = i % S::STAGES;
                 const uint32_t ph = (i / S::STAGES) & 1;
                 if (!mbar_wait(&empty_bar[s], ph ^ 1)) {
                     set_status(a.status, SDV_ERR_DEVICE_TIMEOUT);
+                    timed_out = true;
                     break;
                 }
                 mbar_arrive_expect_tx(&full_bar[s], S::STAGE_BYTES);
@@ -476,6 +486,13 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 const int kc = (kb0 + i) * 64;
                 load_a<KIND>(sa, &tmA0, &tmA1, &tmA2, &full_bar[s], a, tile, kc, pol_w);
                 tma_load_3d(sa + S::A_BYTES, &tmB, &full_bar[s], kc, 0, 0);
+                issued = i + 1;
+            }
+            if (timed_out) {
+                // error path: the copies already issued must land before this CTA may leave (its
+                // shared memory goes to the next CTA); each stage's last issued phase, bounded
+                for (int j = max(0, issued - S::STAGES); j < issued; ++j)
+                    if (!mbar_wait(&full_bar[j % S::STAGES], (j / S::STAGES) & 1)) break;
             }
         }
     } else if (warp == 5) {

@@ -12,7 +12,6 @@
 #include "attention.cuh"
 #include "attention_group.cuh"
 #include "common.cuh"
-#include "fwd.cuh"
 #include "gemm.cuh"
 #include "small.cuh"
 
@@ -44,41 +43,6 @@ int next_pow2(int v) {
     int p = 1;
     while (p < v) p <<= 1;
     return p;
-}
-
-// Most CTAs that share one tile of a plan when its (tile, k-block) units are cut evenly over G CTAs.
-// Split-tile holder table of one plan: [tiles + 1] offsets, then for each tile the partial slots
-// (2c for CTA c's first segment, 2c + 1 for its last) of the CTAs holding its units, in CTA order.
-void holder_table(int tiles, int k_blocks, int G, std::vector<int> &out) {
-    const long long U = static_cast<long long>(tiles) * k_blocks;
-    std::vector<int> off(tiles + 1), slots;
-    for (int t = 0; t < tiles; ++t) {
-        off[t] = static_cast<int>(slots.size());
-        for (long long u = static_cast<long long>(t) * k_blocks; u < static_cast<long long>(t + 1) * k_blocks;) {
-            const long long cc = ((u + 1) * G - 1) / U;
-            const long long first_tile = (cc * U / G) / k_blocks;
-            slots.push_back(static_cast<int>(2 * cc + (t == first_tile ? 0 : 1)));
-            u = (cc + 1) * U / G;
-        }
-    }
-    off[tiles] = static_cast<int>(slots.size());
-    out.insert(out.end(), off.begin(), off.end());
-    out.insert(out.end(), slots.begin(), slots.end());
-}
-
-int max_holders(int tiles, int k_blocks, int G) {
-    const long long U = static_cast<long long>(tiles) * k_blocks;
-    int best = 0;
-    for (int t = 0; t < tiles; ++t) {
-        int n = 0;
-        for (long long u = static_cast<long long>(t) * k_blocks; u < static_cast<long long>(t + 1) * k_blocks;) {
-            const long long cc = ((u + 1) * G - 1) / U;
-            ++n;
-            u = (cc + 1) * U / G;
-        }
-        best = std::max(best, n);
-    }
-    return best;
 }
 
 GemmPlan make_plan(int tiles, int k_blocks, int sm_count) {
@@ -118,24 +82,8 @@ struct sdv_ctx {
     int *attn_cnt = nullptr;
     int attn_splits = 1;
     int attn_lo = 1;  // attention products with hi/lo pairs (queries and probabilities)
-    // persistent forward
-    bool use_fwd = true, fwd_coop = true;
-    int *fwd_sync = nullptr, *fwd_done = nullptr, *fwd_tile_cnt = nullptr, *fwd_att_cnt = nullptr;
-    int *fwd_abort = nullptr, *fwd_n_items = nullptr;
-    int n_sync = 0, fwd_item_cap = 0, fwd_rps = 0, fwd_max_slices = 0, fwd_tile_stride = 0;
-    int4 *fwd_items = nullptr;
-    float *fwd_part = nullptr, *fwd_att_o = nullptr;
-    float2 *fwd_att_ml = nullptr;
-    CUtensorMap *fwd_tm = nullptr;   // device table: per layer wq wk wv wo wg wu wd, LM head, then B maps [4][3]
-    FwdLayer *fwd_layers = nullptr;  // device table
-    int *fwd_hold = nullptr;         // device table of split-tile holders (FwdParams::hold)
-    int fwd_hold_base[5] = {0, 0, 0, 0, 0};
-    std::vector<int> fwd_hold_host;
-    int fwd_ring = 0;                         // ring stages in use, 0 = all
-    unsigned long long *fwd_trace = nullptr;  // caller's timeline buffer, or nullptr
-    size_t fwd_trace_words = 0;
-    std::vector<CUtensorMap> fwd_tm_host;
-    std::vector<FwdLayer> fwd_layers_host;
+    unsigned long long *trace = nullptr;  // caller's timeline buffer (sdv_fwd_trace), or nullptr
+    size_t trace_words = 0;
     int ss_tiles = 0, grp = 0, qrows = 0, work_cap = 0, pages_per_seq = 0, ng_slots = 0;
     size_t layer_stride = 0;  // pool elements per layer
     GemmPlan plan[5];         // qkv, o, gate/up, down, lm head
@@ -194,10 +142,11 @@ struct PhaseMark {
 namespace {
 
 enum { P_QKV = 0, P_O = 1, P_GU = 2, P_DOWN = 3, P_LM = 4 };
-constexpr int kPlans = 5;
-// Timeline buffer on the per-projection path: region 0 for the attention CTAs, region 1 + p for
-// the GEMM launches of plan p; each region holds 16 stamps for up to kTraceRegionCtas CTAs.
+// Timeline buffer (sdv_fwd_trace): one region of kTraceRegionCtas x 16 stamps per launch of a
+// step. Layer l uses regions 5l (attention) and 5l + 1 + p (GEMM of plan p, p < 4); the LM head
+// uses region 5 n_layers.
 constexpr int kTraceRegionCtas = 2048;
+constexpr size_t kTraceRegionWords = static_cast<size_t>(kTraceRegionCtas) * 16;
 
 // Carve the workspace. With ctx == nullptr only the size is computed.
 size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8_t *base, int sm_count) {
@@ -285,30 +234,6 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     float2 *apml = reinterpret_cast<float2 *>(take(sizeof(float2) * nslots));
     int *acnt = reinterpret_cast<int *>(take(sizeof(int) * static_cast<size_t>(B) * m.n_kv_heads * kAttnCluster));
 
-    // persistent forward: completion counters, split-tile counters, attention counters and the
-    // abort flag in one zeroed range; attention items and partials; split-tile partials; tables
-    const int rps = std::max(1, kFwdRows / grp);
-    const int max_slices = ceil_div(c.max_span, rps);
-    const int fchunk_cap = ceil_div(static_cast<long long>(c.n_pages) * c.page_size, kFwdChunk) + B;
-    const int item_cap = fchunk_cap * max_slices;
-    int tile_stride = 0;
-    for (const GemmPlan &p : plans) tile_stride = std::max(tile_stride, p.tiles);
-    const int n_done = 5 * m.n_layers + 1;
-    const int n_att_cnt = B * max_slices * m.n_kv_heads;
-    const int n_sync = n_done + 5 * tile_stride + n_att_cnt + 1;
-    int *fsync = reinterpret_cast<int *>(take(sizeof(int) * static_cast<size_t>(n_sync)));
-    int4 *fitems = reinterpret_cast<int4 *>(take(sizeof(int4) * static_cast<size_t>(item_cap)));
-    int *fn_items = reinterpret_cast<int *>(take(sizeof(int)));
-    float *fpart = reinterpret_cast<float *>(take(sizeof(float) * 2 * static_cast<size_t>(sm_count) * kRowsCap * 128));
-    const size_t att_slots = static_cast<size_t>(item_cap) * m.n_kv_heads * kFwdRows;
-    float *fatt_o = reinterpret_cast<float *>(take(sizeof(float) * att_slots * D));
-    float2 *fatt_ml = reinterpret_cast<float2 *>(take(sizeof(float2) * att_slots));
-    CUtensorMap *ftm = reinterpret_cast<CUtensorMap *>(take(sizeof(CUtensorMap) * (7 * m.n_layers + 1 + 12)));
-    FwdLayer *flay = reinterpret_cast<FwdLayer *>(take(sizeof(FwdLayer) * m.n_layers));
-    size_t n_hold = 0;
-    for (const GemmPlan &p : plans) n_hold += 2 * static_cast<size_t>(p.tiles) + 1 + sm_count;
-    int *fhold = reinterpret_cast<int *>(take(sizeof(int) * n_hold));
-
     if (ctx) {
         ctx->st = s;
         ctx->x = x;
@@ -329,24 +254,6 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
         ctx->attn_pml = apml;
         ctx->attn_cnt = acnt;
         ctx->attn_splits = splits;
-        ctx->fwd_sync = fsync;
-        ctx->n_sync = n_sync;
-        ctx->fwd_done = fsync;
-        ctx->fwd_tile_cnt = fsync + n_done;
-        ctx->fwd_att_cnt = fsync + n_done + 5 * tile_stride;
-        ctx->fwd_abort = fsync + n_done + 5 * tile_stride + n_att_cnt;
-        ctx->fwd_items = fitems;
-        ctx->fwd_n_items = fn_items;
-        ctx->fwd_item_cap = item_cap;
-        ctx->fwd_rps = rps;
-        ctx->fwd_max_slices = max_slices;
-        ctx->fwd_tile_stride = tile_stride;
-        ctx->fwd_part = fpart;
-        ctx->fwd_att_o = fatt_o;
-        ctx->fwd_att_ml = fatt_ml;
-        ctx->fwd_tm = ftm;
-        ctx->fwd_layers = flay;
-        ctx->fwd_hold = fhold;
         ctx->ss_tiles = ss_tiles;
         ctx->grp = grp;
         ctx->qrows = qrows;
@@ -551,7 +458,13 @@ cudaError_t set_gemm_smem() {
 
 int rc(cudaError_t e) { return e == cudaSuccess ? SDV_OK : SDV_ERR_CUDA; }
 
-GemmArgs base_args(const sdv_ctx *ctx, int kind, int pidx) {
+// Stamps of launch `region` of the step, or nullptr when tracing is off or the launch has too many CTAs.
+unsigned long long *trace_region(const sdv_ctx *ctx, int region, size_t ctas) {
+    if (!ctx->trace || ctas > kTraceRegionCtas || ctx->trace_words < kTraceRegionWords * (region + 1)) return nullptr;
+    return ctx->trace + kTraceRegionWords * region;
+}
+
+GemmArgs base_args(const sdv_ctx *ctx, int kind, int pidx, int layer) {
     GemmArgs a{};
     const GemmPlan &p = ctx->plan[pidx];
     a.kind = kind;
@@ -569,11 +482,8 @@ GemmArgs base_args(const sdv_ctx *ctx, int kind, int pidx) {
     a.partial = ctx->part[pidx];
     a.counters = ctx->cnt[pidx];
     a.part_stride = p.tiles * 128;
-    // timeline of the per-projection path: launch kind pidx writes region pidx + 1
-    const size_t region = static_cast<size_t>(kTraceRegionCtas) * 16;
-    if (ctx->fwd_trace && ctx->fwd_trace_words >= region * (kPlans + 1) &&
-        static_cast<size_t>(p.tiles) * p.splits <= kTraceRegionCtas)
-        a.trace = ctx->fwd_trace + region * (pidx + 1);
+    a.trace = trace_region(ctx, pidx == P_LM ? 5 * ctx->m.n_layers : 5 * layer + 1 + pidx,
+                           static_cast<size_t>(p.tiles) * p.splits);
     return a;
 }
 
@@ -605,9 +515,8 @@ int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *
     a.status = ctx->st.status;
     a.splits = ctx->attn_splits;
     a.layer = layer;
-    // the timeline buffer of sdv_fwd_trace, when set: 16 stamps per CTA in region 0
-    if (static_cast<size_t>(ctx->work_cap) * ctx->attn_splits * m.n_kv_heads <= kTraceRegionCtas)
-        a.trace = ctx->fwd_trace;
+    // the timeline buffer of sdv_fwd_trace, when set (the TMA-fed kernel writes it)
+    a.trace = trace_region(ctx, 5 * layer, static_cast<size_t>(ctx->work_cap) * ctx->attn_splits * m.n_kv_heads);
     a.p_lo = ctx->attn_lo;
     if (!ctx->attn_lo) a.q_plane = 0;  // queries as bf16 only
     if (!ctx->attn_tma) {  // 8-CTA clusters per 1024-position group (attention.cuh)
@@ -665,20 +574,13 @@ int prepare(sdv_ctx *ctx, const int32_t *tokens, const int32_t *row_off, const i
     p.H = ctx->m.hidden;
     p.vocab = ctx->m.vocab;
     p.rows_cap = kRowsCap;
-    p.items = ctx->fwd_items;
-    p.n_items = ctx->fwd_n_items;
-    p.item_cap = ctx->fwd_item_cap;
-    p.item_keys = kFwdChunk;
-    p.rps = ctx->fwd_rps;
-    p.zero = ctx->fwd_sync;
-    p.n_zero = ctx->n_sync;
     return rc(launch(ctx, prepare_kernel, dim3(embed ? 1 + max_rows : 1), dim3(128), 0, st, p));
 }
 
-// Epilogue arguments of the projections, without the per-layer fields.
-GemmArgs qkv_args(const sdv_ctx *ctx) {
+// Arguments of the QKV projection of layer l (q/k head norm, RoPE, paged K/V write).
+GemmArgs qkv_args(const sdv_ctx *ctx, int l) {
     const sdv_model_cfg &m = ctx->m;
-    GemmArgs a = base_args(ctx, EPI_QKV, P_QKV);
+    GemmArgs a = base_args(ctx, EPI_QKV, P_QKV, l);
     a.n_out = (m.n_q_heads + 2 * m.n_kv_heads) * m.head_dim;
     a.nq = m.n_q_heads;
     a.nkv = m.n_kv_heads;
@@ -695,95 +597,10 @@ GemmArgs qkv_args(const sdv_ctx *ctx) {
     a.page_size = ctx->c.page_size;
     a.n_pages = ctx->c.n_pages;
     a.q_out = ctx->q;
+    a.q_gain = static_cast<const bf16 *>(ctx->layers[l].q_norm);
+    a.k_gain = static_cast<const bf16 *>(ctx->layers[l].k_norm);
+    a.kv_layer = ctx->pool + ctx->layer_stride * l;
     return a;
-}
-
-template <int N, int D>
-cudaError_t launch_fwd_nd(const sdv_ctx *ctx, const FwdParams &P, cudaStream_t st) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(P.grid);
-    cfg.blockDim = dim3(kFwdThreads);
-    cfg.dynamicSmemBytes = FwdShape<N, D>::SMEM_BYTES;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = ctx->fwd_coop ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, fwd_kernel<N, D>, P);
-}
-
-template <int D>
-cudaError_t launch_fwd_d(const sdv_ctx *ctx, int nidx, const FwdParams &P, cudaStream_t st) {
-    switch (nidx) {
-        case 0: return launch_fwd_nd<16, D>(ctx, P, st);
-        case 1: return launch_fwd_nd<32, D>(ctx, P, st);
-        case 2: return launch_fwd_nd<64, D>(ctx, P, st);
-        default: return launch_fwd_nd<128, D>(ctx, P, st);
-    }
-}
-
-// Every layer and the LM head in one persistent launch (fwd.cuh).
-int launch_fwd(sdv_ctx *ctx, int nidx, int32_t *d_argmax, float *d_logits, cudaStream_t st) {
-    const sdv_model_cfg &m = ctx->m;
-    FwdParams P{};
-    P.tm_w = ctx->fwd_tm;
-    P.tm_b = ctx->fwd_tm + 7 * m.n_layers + 1 + 3 * nidx;
-    P.layers = ctx->fwd_layers;
-    P.n_layers = m.n_layers;
-    P.grid = ctx->sm_count;
-    for (int i = 0; i < 5; ++i) P.g[i] = FwdGemm{ctx->plan[i].tiles, ctx->plan[i].k_blocks};
-    P.ga[EPI_QKV] = qkv_args(ctx);
-    GemmArgs r = base_args(ctx, EPI_RESID, P_O);
-    r.n_out = m.hidden;
-    r.x = ctx->x;
-    r.xb = ctx->xb;
-    r.ss_out = ctx->ss;
-    P.ga[EPI_RESID] = r;
-    GemmArgs g = base_args(ctx, EPI_SWIGLU, P_GU);
-    g.n_out = m.ffn;
-    g.h_out = ctx->h;
-    P.ga[EPI_SWIGLU] = g;
-    GemmArgs lm = base_args(ctx, EPI_LMHEAD, P_LM);
-    lm.keys = ctx->keys;
-    lm.logits = d_logits;
-    lm.argmax_out = d_argmax;
-    lm.vocab = m.vocab;
-    P.ga[EPI_LMHEAD] = lm;
-    P.layer_stride = ctx->layer_stride;
-    P.pool = ctx->pool;
-    P.attn_out = ctx->attn_o;
-    P.q_plane = static_cast<size_t>(kRowsCap) * m.n_q_heads * m.head_dim;
-    P.items = ctx->fwd_items;
-    P.n_items = ctx->fwd_n_items;
-    P.row_off = ctx->st.row_off;
-    P.rps = ctx->fwd_rps;
-    P.page_shift = __builtin_ctz(static_cast<unsigned>(ctx->c.page_size));
-    P.max_slices = ctx->fwd_max_slices;
-    P.scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(m.head_dim));
-    P.att_o = ctx->fwd_att_o;
-    P.att_ml = ctx->fwd_att_ml;
-    P.att_cnt = ctx->fwd_att_cnt;
-    P.done = ctx->fwd_done;
-    P.tile_cnt = ctx->fwd_tile_cnt;
-    P.tile_stride = ctx->fwd_tile_stride;
-    P.part = ctx->fwd_part;
-    P.abort_flag = ctx->fwd_abort;
-    P.trace = ctx->fwd_trace;
-    P.hold = ctx->fwd_hold;
-    for (int i = 0; i < 5; ++i) P.hold_base[i] = ctx->fwd_hold_base[i];
-    P.ring = ctx->fwd_ring;
-    const cudaError_t e = m.head_dim == 128 ? launch_fwd_d<128>(ctx, nidx, P, st) : launch_fwd_d<64>(ctx, nidx, P, st);
-    return rc(e);
-}
-
-template <int D>
-cudaError_t set_fwd_smem_d() {
-    cudaError_t e = set_smem(fwd_kernel<16, D>, FwdShape<16, D>::SMEM_BYTES);
-    if (e == cudaSuccess) e = set_smem(fwd_kernel<32, D>, FwdShape<32, D>::SMEM_BYTES);
-    if (e == cudaSuccess) e = set_smem(fwd_kernel<64, D>, FwdShape<64, D>::SMEM_BYTES);
-    if (e == cudaSuccess) e = set_smem(fwd_kernel<128, D>, FwdShape<128, D>::SMEM_BYTES);
-    return e;
 }
 
 }  // namespace
@@ -897,66 +714,9 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
     if (e == cudaSuccess) e = set_smem(attn_kernel<64>, AttnShape<64>::SMEM);
     if (e == cudaSuccess) e = set_smem(attn_group_kernel<128>, GrpShape<128>::SMEM);
     if (e == cudaSuccess) e = set_smem(attn_group_kernel<64>, GrpShape<64>::SMEM);
-    if (e == cudaSuccess) e = D == 128 ? set_fwd_smem_d<128>() : set_fwd_smem_d<64>();
     if (e != cudaSuccess) {
         delete ctx;
         return SDV_ERR_CUDA;
-    }
-
-    // The persistent forward needs one co-resident CTA per SM.
-    {
-        int coop = 0, occ = 0;
-        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-        cudaError_t oe = D == 128 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fwd_kernel<128, 128>, kFwdThreads,
-                                                                                  FwdShape<128, 128>::SMEM_BYTES)
-                                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fwd_kernel<128, 64>, kFwdThreads,
-                                                                                  FwdShape<128, 64>::SMEM_BYTES);
-        if (oe != cudaSuccess) cudaGetLastError();
-        ctx->fwd_coop = coop != 0;
-        ctx->use_fwd = oe == cudaSuccess && occ >= 1;
-        // SDV_FORWARD=persistent selects the persistent forward; the default is one launch per projection
-        const char *ev = std::getenv("SDV_FORWARD");
-        if (!(ev && std::strcmp(ev, "persistent") == 0)) ctx->use_fwd = false;
-        if (c->page_size & (c->page_size - 1)) ctx->use_fwd = false;  // page index by shift
-        // the kernel's unit arithmetic is 32-bit, and a split tile's partials must fit its staging region
-        const int att = D == 128 ? FwdShape<128, 128>::STAGE_BYTES : FwdShape<128, 64>::STAGE_BYTES;
-        for (int i = 0; i < 5; ++i) {
-            const long long U = static_cast<long long>(ctx->plan[i].tiles) * ctx->plan[i].k_blocks;
-            if (U * (sms + 1) >= (1ll << 31)) ctx->use_fwd = false;
-            const int mh = max_holders(ctx->plan[i].tiles, ctx->plan[i].k_blocks, sms);
-            if (mh > kFwdMaxHolders || (mh + 1) * 512 > att) ctx->use_fwd = false;  // + the staged residual rows
-        }
-    }
-    ctx->fwd_tm_host.resize(7 * m->n_layers + 1 + 12);
-    for (int l = 0; l < m->n_layers; ++l) {
-        CUtensorMap *t = &ctx->fwd_tm_host[7 * l];
-        t[0] = ctx->tm_wq[l];
-        t[1] = ctx->tm_wk[l];
-        t[2] = ctx->tm_wv[l];
-        t[3] = ctx->tm_wo[l];
-        t[4] = ctx->tm_wg[l];
-        t[5] = ctx->tm_wu[l];
-        t[6] = ctx->tm_wd[l];
-    }
-    ctx->fwd_tm_host[7 * m->n_layers] = ctx->tm_lm;
-    for (int i = 0; i < 4; ++i) {
-        CUtensorMap *t = &ctx->fwd_tm_host[7 * m->n_layers + 1 + 3 * i];
-        t[0] = ctx->tm_xb[i];
-        t[1] = ctx->tm_ao[i];
-        t[2] = ctx->tm_h[i];
-    }
-    ctx->fwd_hold_host.clear();
-    for (int i = 0; i < 5; ++i) {
-        ctx->fwd_hold_base[i] = static_cast<int>(ctx->fwd_hold_host.size());
-        holder_table(ctx->plan[i].tiles, ctx->plan[i].k_blocks, sms, ctx->fwd_hold_host);
-    }
-    ctx->fwd_layers_host.resize(m->n_layers);
-    for (int l = 0; l < m->n_layers; ++l) {
-        FwdLayer &f = ctx->fwd_layers_host[l];
-        f.q_gain = static_cast<const bf16 *>(ctx->layers[l].q_norm);
-        f.k_gain = static_cast<const bf16 *>(ctx->layers[l].k_norm);
-        f.ffn_norm = static_cast<const bf16 *>(ctx->layers[l].ffn_norm);
-        f.next_norm = static_cast<const bf16 *>(l + 1 < m->n_layers ? ctx->layers[l + 1].attn_norm : w->final_norm);
     }
 
     // RoPE table: cos/sin of pos * theta^(-2j/D), in double on the host.
@@ -973,15 +733,6 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
     e = cudaMemsetAsync(ctx->ws, 0, ws_bytes, st);
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(ctx->rope, ctx->rope_host.data(), ctx->rope_host.size() * sizeof(float2),
-                            cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(ctx->fwd_tm, ctx->fwd_tm_host.data(), ctx->fwd_tm_host.size() * sizeof(CUtensorMap),
-                            cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(ctx->fwd_layers, ctx->fwd_layers_host.data(), ctx->fwd_layers_host.size() * sizeof(FwdLayer),
-                            cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(ctx->fwd_hold, ctx->fwd_hold_host.data(), ctx->fwd_hold_host.size() * sizeof(int),
                             cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) {
         init_state_kernel<<<64, 256, 0, st>>>(ctx->st);
@@ -1021,33 +772,10 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
         r = prepare(ctx, d_tokens, d_row_off, nullptr, B, max_rows, max_span, 1, st);
     }
     if (r) return r;
-    if (ctx->use_fwd) {
-        PhaseMark pm(ctx, 7, st);
-        return launch_fwd(ctx, ni, d_argmax, d_logits, st);
-    }
     for (int l = 0; l < m.n_layers; ++l) {
         const sdv_layer_weights &L = ctx->layers[l];
         // QKV projection + q/k head norm + RoPE + paged K/V write
-        GemmArgs a = base_args(ctx, EPI_QKV, P_QKV);
-        a.n_out = (m.n_q_heads + 2 * m.n_kv_heads) * m.head_dim;
-        a.nq = m.n_q_heads;
-        a.nkv = m.n_kv_heads;
-        a.D = m.head_dim;
-        a.q_tiles = m.n_q_heads * m.head_dim / 128;
-        a.k_tiles = m.n_kv_heads * m.head_dim / 128;
-        a.qk_norm = m.qk_norm;
-        a.q_gain = static_cast<const bf16 *>(L.q_norm);
-        a.k_gain = static_cast<const bf16 *>(L.k_norm);
-        a.rope = ctx->rope;
-        a.rope_rows = ctx->c.max_context;
-        a.row_seq = ctx->st.row_seq;
-        a.row_pos = ctx->st.row_pos;
-        a.page_table = ctx->st.page_table;
-        a.pages_per_seq = ctx->pages_per_seq;
-        a.page_size = ctx->c.page_size;
-        a.n_pages = ctx->c.n_pages;
-        a.q_out = ctx->q;
-        a.kv_layer = ctx->pool + ctx->layer_stride * l;
+        GemmArgs a = qkv_args(ctx, l);
         cudaError_t e;
         {
             PhaseMark pm(ctx, 1, st);
@@ -1063,7 +791,7 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
         if (r) return r;
         // O projection + residual; emits bf16(x * g_ffn) and sum-of-squares parts. Its weights
         // (21 MB) are pulled into L2 during the attention, when HBM is otherwise idle.
-        a = base_args(ctx, EPI_RESID, P_O);
+        a = base_args(ctx, EPI_RESID, P_O, l);
         a.l2_ahead = 64;
         a.n_out = m.hidden;
         a.x = ctx->x;
@@ -1077,7 +805,7 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
         }
         if (e != cudaSuccess) return SDV_ERR_CUDA;
         // gate/up projection + SwiGLU
-        a = base_args(ctx, EPI_SWIGLU, P_GU);
+        a = base_args(ctx, EPI_SWIGLU, P_GU, l);
         a.n_out = m.ffn;
         a.h_out = ctx->h;
         {
@@ -1087,7 +815,7 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
         }
         if (e != cudaSuccess) return SDV_ERR_CUDA;
         // down projection + residual; emits bf16(x * g_next) for the next layer (or the final norm)
-        a = base_args(ctx, EPI_RESID, P_DOWN);
+        a = base_args(ctx, EPI_RESID, P_DOWN, l);
         a.n_out = m.hidden;
         a.x = ctx->x;
         a.xb = ctx->xb;
@@ -1101,7 +829,7 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
         if (e != cudaSuccess) return SDV_ERR_CUDA;
     }
     // final norm (folded as a per-row scale) + LM head + per-row argmax
-    GemmArgs a = base_args(ctx, EPI_LMHEAD, P_LM);
+    GemmArgs a = base_args(ctx, EPI_LMHEAD, P_LM, 0);
     a.keys = ctx->keys;
     a.logits = d_logits;
     a.argmax_out = d_argmax;
@@ -1237,7 +965,7 @@ int sdv_profile_read(sdv_ctx *ctx, float *h_ms, int32_t *h_count) {
         float ms = 0.f;
         if (cudaEventElapsedTime(&ms, ctx->ev_pool[mk.second.first], ctx->ev_pool[mk.second.second]) != cudaSuccess)
             return SDV_ERR_CUDA;
-        if (mk.first >= 0 && mk.first < 8) {
+        if (mk.first >= 0 && mk.first < 7) {
             h_ms[mk.first] += ms;
             h_count[mk.first] += 1;
         }
@@ -1250,13 +978,15 @@ int sdv_profile_read(sdv_ctx *ctx, float *h_ms, int32_t *h_count) {
 int sdv_fwd_trace(sdv_ctx *ctx, void *d_buf, size_t bytes) {
     if (!ctx) return SDV_ERR_ARG;
     if (!d_buf) {
-        ctx->fwd_trace = nullptr;
+        ctx->trace = nullptr;
+        ctx->trace_words = 0;
         return SDV_OK;
     }
-    const size_t need = static_cast<size_t>(ctx->sm_count) * (5 * ctx->m.n_layers + 1) * 16 * sizeof(unsigned long long);
-    if (bytes < need || reinterpret_cast<uintptr_t>(d_buf) % 8) return SDV_ERR_ARG;
-    ctx->fwd_trace = static_cast<unsigned long long *>(d_buf);
-    ctx->fwd_trace_words = bytes / sizeof(unsigned long long);
+    if (reinterpret_cast<uintptr_t>(d_buf) % 8) return SDV_ERR_ARG;
+    // at least the attention and GEMM regions of the first layer
+    if (bytes < kTraceRegionWords * 5 * sizeof(unsigned long long)) return SDV_ERR_ARG;
+    ctx->trace = static_cast<unsigned long long *>(d_buf);
+    ctx->trace_words = bytes / sizeof(unsigned long long);
     return SDV_OK;
 }
 

@@ -79,13 +79,6 @@ struct PrepArgs {
     float *ss;           // [ss_tiles][rows_cap]
     unsigned long long *keys;  // [rows_cap]
     int H, vocab, rows_cap;
-    // persistent forward: attention items (b | slice << 16, chunk | n_chunks << 16, L_b, S_b) of
-    // `item_keys` keys and `rps` span rows each, and the counters zeroed before every forward
-    int4 *items;
-    int *n_items;
-    int item_cap, item_keys, rps;
-    int *zero;
-    int n_zero;
 };
 
 // Block 0: validate the spans, record bases/offsets/row maps, advance lengths,
@@ -96,14 +89,12 @@ __global__ void prepare_kernel(PrepArgs p) {
     DevState &s = p.s;
     __shared__ int ok_s;
     __shared__ int wo_s[257];
-    __shared__ int io_s[257];
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.n_zero; i += gridDim.x * blockDim.x) p.zero[i] = 0;
     if (blockIdx.x == 0) {
         if (threadIdx.x == 0) {
             int ok = p.row_off[0] == 0;
             int R = p.row_off[p.B];
             if (R < 0 || R > p.max_rows) ok = 0;
-            int nw = 0, ni_tot = 0;
+            int nw = 0;
             for (int b = 0; b < p.B && ok; ++b) {
                 const int S = p.row_off[b + 1] - p.row_off[b];
                 if (S < 0 || S > p.max_span) {
@@ -120,27 +111,18 @@ __global__ void prepare_kernel(PrepArgs p) {
                 }
                 wo_s[b] = nw;
                 nw += S > 0 ? (L + S + p.chunk - 1) / p.chunk : 0;
-                io_s[b] = ni_tot;
-                for (int q0 = 0; q0 < S; q0 += p.rps) {
-                    const int key_end = L + q0 + min(S - q0, p.rps);
-                    ni_tot += (key_end + p.item_keys - 1) / p.item_keys;
-                }
             }
             if (ok && nw > s.work_cap) ok = 0;
-            if (ok && ni_tot > p.item_cap) ok = 0;
             if (!ok) {
                 set_status(s.status, SDV_ERR_ARG);
                 R = 0;
                 nw = 0;
-                ni_tot = 0;
-                for (int b = 0; b <= p.B; ++b) wo_s[b] = io_s[b] = 0;
+                for (int b = 0; b <= p.B; ++b) wo_s[b] = 0;
             }
             wo_s[p.B] = nw;
-            io_s[p.B] = ni_tot;
             ok_s = ok;
             *s.nrows = R;
             *s.n_work = nw;
-            *p.n_items = ni_tot;
         }
         __syncthreads();
         const int ok = ok_s;
@@ -167,17 +149,6 @@ __global__ void prepare_kernel(PrepArgs p) {
             const int L = p.base ? p.base[b] : s.seq_base[b];
             const int r0 = p.row_off[b], S = p.row_off[b + 1] - r0;
             for (int c = threadIdx.x; c < n; c += blockDim.x) s.work[w0 + c] = make_int4(b | (c << 16), L, S, r0);
-        }
-        for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
-            if (io_s[b + 1] == io_s[b]) continue;
-            const int L = p.base ? p.base[b] : s.seq_base[b];
-            const int S = p.row_off[b + 1] - p.row_off[b];
-            int i = io_s[b];
-            for (int q0 = 0, qs = 0; q0 < S; q0 += p.rps, ++qs) {
-                const int key_end = L + q0 + min(S - q0, p.rps);
-                const int nch = (key_end + p.item_keys - 1) / p.item_keys;
-                for (int ch = 0; ch < nch; ++ch) p.items[i++] = make_int4(b | (qs << 16), ch | (nch << 16), L, S);
-            }
         }
         for (int r = threadIdx.x; r < p.rows_cap; r += blockDim.x) p.keys[r] = 0ull;
         return;
