@@ -8,12 +8,15 @@ verify steps of S = K+1 = 8 rows with uniform-random drafts. A step is the
 whole hot path: propose -> ensure_capacity -> spec_forward (verify) ->
 accept_greedy -> rewind_cache, replayed as one CUDA graph.
 
-Metric: committed tokens/s (whole job, all GPUs). Also reported: ms per step,
-the per-S latency sweep (S = 1..17), the HBM roofline of the dominant kernel
-(the tcgen05 weight-streaming GEMM), the end-to-end figure through host
-buffers, and the CPU oracle timed on the host cores.
+Metric: committed tokens/s (whole job, all GPUs). The JSON line also carries
+the batch-16 (contexts U[512, 4096]) and 32768-token-context lines as
+sub-objects, the per-S latency sweep (S = 1..17), the HBM roofline of the
+dominant kernel (the tcgen05 weight-streaming GEMM) timed inside the captured
+step from the device timeline, the end-to-end figure through host buffers, and
+the CPU oracle timed on the host cores in a fresh process.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload b1|b16|ctx32k|ngram] [--no-extra] [--no-sweep] [--no-cpu-baseline]
 """
 from __future__ import annotations
 
@@ -34,17 +37,22 @@ sys.path.insert(0, ROOT)
 CONTEXT = 848
 K_DRAFT = 7
 SEED = 2
-WEIGHT_BYTES_PER_STEP = 8_044_936_192      # 36 layers + LM head + final norm (bf16)
+N_LAYERS = 36
+# Weight bytes of one forward (bf16): per layer the four GEMMs' matrices
+# (q/k/v 6144 x 2560, o 2560 x 4096, gate+up 2 x 9728 x 2560, down 2560 x 9728) and the four norm
+# gains; then the LM head (151936 x 2560) and the final norm.
+GEMM_BYTES_PER_LAYER = 201_850_880
+GEMM_BYTES = {"qkv": 31_457_280, "o": 20_971_520, "gate_up": 99_614_720, "down": 49_807_360,
+              "lm_head": 777_912_320}
+WEIGHT_BYTES_PER_STEP = 8_044_936_192      # 36 x (201,850,880 + 10,752 norm gains) + LM head + final norm
 KV_BYTES_PER_TOKEN = 147_456               # 2 (K,V) x 8 heads x 128 x 2 B x 36 layers
-# DRAM bytes (read + write) that ncu measured per launch of the weight-streaming GEMM on the
-# per-projection path, in a 2-layer case of the same shapes (every launch of two timed steps):
-# QKV, O, gate/up, down per layer, then the LM head.
-# A launch streams its own weights, so a 36-layer step is 36 layers of the first four plus one
-# LM head; divided by the 145 launches it is the per-launch traffic beside `achieved`.
-GEMM_TRAFFIC_MB = {"qkv": 31.6998, "o": 21.3698, "gate_up": 99.9877, "down": 50.5655, "lm_head": 778.2215}
-GEMM_TRAFFIC_PER_LAUNCH = (36 * (GEMM_TRAFFIC_MB["qkv"] + GEMM_TRAFFIC_MB["o"] + GEMM_TRAFFIC_MB["gate_up"] +
-                                 GEMM_TRAFFIC_MB["down"]) + GEMM_TRAFFIC_MB["lm_head"]) * 1e6 / 145
 EMBED_BYTES_PER_ROW = 2560 * 2
+# DRAM bytes (read + write) that ncu measured per launch of the weight-streaming GEMM, in a
+# 2-layer case of the same shapes (profiles/gemm_tcgen05_qwen3_4b_verify_N16.md); a launch streams
+# its own weights, so a 36-layer step is 36 layers of the first four plus one LM head.
+GEMM_TRAFFIC_MB = {"qkv": 31.6998, "o": 21.3698, "gate_up": 99.9877, "down": 50.5655, "lm_head": 778.2215}
+TRACE_REGION_WORDS = 2048 * 16            # sdv_fwd_trace: 16 stamps x 2048 CTAs per launch
+PROJ = ("qkv", "o", "gate_up", "down")
 
 
 def peaks():
@@ -78,7 +86,7 @@ class ClockSampler:
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index):
         self.idx = gpu_index
         self.proc = None
         self.path = None
@@ -119,19 +127,63 @@ class ClockSampler:
                 "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
 
 
-# ----------------------------------------------------------------------------- our implementation
+# ----------------------------------------------------------------------------- helpers
 
 def build_weights(shape, seed, device="cuda"):
     import synth
     from speculative_decoding_verify_02_gb300 import upload_bf16
-    host, dev = {}, {}
+    dev = {}
     for name in shape.tensor_shapes():
-        host[name] = synth.tensor(shape, seed, name)
-        dev[name] = upload_bf16(host[name], device)
-    return host, dev
+        dev[name] = upload_bf16(synth.tensor(shape, seed, name), device)
+    return dev
 
 
-def run_ours(args, rank, world):
+def timed_replays(loop, steps, stream):
+    """Device time (ms) of `steps` graph replays, CUDA events on the launching stream."""
+    import torch
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        loop.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def trace_launches(buf, n_layers):
+    """Per-launch spans of the last traced step from the device timeline: for each launch, the
+    first CTA start to the last CTA end (ns). Returns {"gemm": {proj: [per layer]}, "lm_head": ns,
+    "attention": [per layer], "gemm_detail": {proj: medians of the launch phases}}."""
+    t = buf.view(-1, 2048, 16).cpu().numpy()
+    first = t[1, :, 0]
+    t0 = int(first[first > 0].min())          # every CTA of layer 0's QKV launch runs each step
+
+    def span(region, ev_end):
+        st, en = t[region, :, 0], t[region, :, ev_end]
+        ok = (st >= t0) & (en >= st)
+        return int(en[ok].max() - st[ok].min()) if ok.any() else 0
+
+    def phases(region):
+        st, ok = t[region, :, 0], t[region, :, 0] >= t0
+        c = t[region][ok]
+        s0 = int(c[:, 0].min())
+        return {"ready": int(c[:, 1].max() - s0), "first_stage": int(c[:, 2].max() - s0),
+                "last_mma": int(c[:, 3].max() - s0), "acc_ready": int(c[:, 4].max() - s0),
+                "reduced": int(c[:, 6].max() - s0), "end": int(c[:, 8].max() - s0)}
+
+    gemm = {p: [span(5 * l + 1 + i, 8) for l in range(n_layers)] for i, p in enumerate(PROJ)}
+    detail = {}
+    for i, p in enumerate(PROJ):
+        ph = [phases(5 * l + 1 + i) for l in range(n_layers)]
+        detail[p] = {k: round(statistics.median(x[k] for x in ph) / 1e3, 2) for k in ph[0]}
+    return {"gemm": gemm, "lm_head": span(5 * n_layers, 8),
+            "attention": [span(5 * l, 6) for l in range(n_layers)], "gemm_detail_us": detail}
+
+
+# ----------------------------------------------------------------------------- the headline (b1)
+
+def run_ours(args, rank, world, dev):
     import torch
     import synth
     from synth import workloads
@@ -139,12 +191,10 @@ def run_ours(args, rank, world):
     from speculative_decoding_verify_02_gb300.runner import SpecLoop
 
     dev_index = int(os.environ.get("LOCAL_RANK", 0))
-    torch.cuda.set_device(dev_index)
     shape = synth.QWEN3_4B if args.layers <= 0 else synth.QWEN3_4B.with_layers(args.layers)
     t_setup = time.time()
-    host, dev = build_weights(shape, SEED)
     sweep_steps = 8 if args.sweep else 0
-    total_steps = args.warmup + args.steps + 2 * args.steps + 17 * (sweep_steps + 3) + 16
+    total_steps = 2 * args.warmup + 4 * args.steps + 17 * (sweep_steps + 3) + 16
     max_ctx = CONTEXT + total_steps * 17 + 256
     n_pages = -(-max_ctx // 16) + 8
     v = Verifier(shape, dev, page_size=16, n_pages=n_pages, max_batch=1, max_rows=128, max_span=128,
@@ -180,30 +230,40 @@ def run_ours(args, rank, world):
     L0 = cache_len()
     ctx_start = L0
     s = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_push("timed")           # profilers can select the timed steps by this range
-    e0.record(s)
-    for _ in range(args.steps):
-        loop.replay()
-    e1.record(s)
+    ms = timed_replays(loop, args.steps, s)
     torch.cuda.nvtx.range_pop()
-    torch.cuda.synchronize()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
     committed = cache_len() - L0
     assert v.get_status() == 0
 
-    # live per-phase kernel timing (events around each launch group, same workload)
+    # The same step captured with the device timeline on (a few %globaltimer stores per CTA):
+    # every launch's first-CTA-start to last-CTA-end inside the graph, PDL overlap included.
+    n_regions = 5 * shape.n_layers + 1
+    trace_buf = torch.zeros(n_regions * TRACE_REGION_WORDS, dtype=torch.int64, device="cuda")
+    v.fwd_trace(trace_buf)
+    tloop = SpecLoop(v, B=1, max_span=K_DRAFT + 1)
+    tloop.first.copy_(loop.committed[:1])
+    tloop.capture(**step_kw)
+    v.fwd_trace(None)
+    for _ in range(args.warmup):
+        tloop.replay()
+    trace_buf.zero_()
+    traced_ms = timed_replays(tloop, args.steps, s)
+    tr = trace_launches(trace_buf, shape.n_layers)
+    assert v.get_status() == 0
+    del trace_buf
+
+    # per-phase kernel time with each launch group run alone (CUDA events around each group,
+    # eager steps): serialised, so it is an upper bound on each kernel's in-graph time
     v.profile_enable(True)
     v.profile_read()
-    prof_ctx0 = cache_len()
     for _ in range(args.steps):
         loop.step(**step_kw)
     prof = v.profile_read()
-    prof_ctx = (prof_ctx0 + cache_len()) / 2
     v.profile_enable(False)
 
     # end to end through host buffers: the step's drafts go up from pinned memory, its result comes back
@@ -239,17 +299,11 @@ def run_ours(args, rank, world):
             lp.capture(drafter=SDV_DRAFT_TABLE, table=table, table_stride=table_len, ngram=False)
             for _ in range(3):
                 lp.replay()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(s)
-            for _ in range(sweep_steps):
-                lp.replay()
-            b.record(s)
-            torch.cuda.synchronize()
-            sweep[S] = round(a.elapsed_time(b) / sweep_steps, 4)
+            sweep[S] = round(timed_replays(lp, sweep_steps, s) / sweep_steps, 4)
         assert v.get_status() == 0
     ctx_end = cache_len()
+    v.close()
 
-    # aggregate over ranks: tokens summed, time = max
     if world > 1:
         committed_all, ms_max, e2e_committed_all, e2e_max = aggregate_replicas(committed, ms, e2e_committed, e2e_s,
                                                                                "cuda")
@@ -258,20 +312,23 @@ def run_ours(args, rank, world):
 
     mean_ctx = (ctx_start + ctx_start + committed) / 2
     S = K_DRAFT + 1
-    step_bytes = WEIGHT_BYTES_PER_STEP + (mean_ctx + S) * KV_BYTES_PER_TOKEN + S * EMBED_BYTES_PER_ROW
+    L = shape.n_layers
+    step_bytes = (L * (GEMM_BYTES_PER_LAYER + 10_752) + GEMM_BYTES["lm_head"] + 5120
+                  + (mean_ctx + S) * KV_BYTES_PER_TOKEN * L / N_LAYERS + S * EMBED_BYTES_PER_ROW)
     peak, peak_kind = peaks()
-    # dominant kernel: the weight-streaming GEMM (every projection and the LM head)
-    gemm_phases = ("qkv_gemm", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm")
-    dom_ms = sum(prof[p][0] for p in gemm_phases)
-    dom_launches = sum(prof[p][1] for p in gemm_phases)
-    dom_bytes = WEIGHT_BYTES_PER_STEP * args.steps + S * 2560 * 2 * 5 * 36 * args.steps
-    dom_name = "gemm_kernel (tcgen05 weight-streaming GEMM, all projections + LM head)"
-    launches_per_step = 4 + 2 + 36 * (1 + 2 + 3)
-    dom_traffic = None
-    if args.layers <= 0 and dom_launches == 145 * args.steps:
-        dom_traffic = round(GEMM_TRAFFIC_PER_LAUNCH / 1e9, 5)   # GB per launch, as `achieved` per second
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    # dominant kernel: the weight-streaming GEMM; algorithmic bytes = the weight matrix each launch
+    # streams; time = each launch's in-graph span from the device timeline, summed over the step
+    gemm_bytes = L * GEMM_BYTES_PER_LAYER + GEMM_BYTES["lm_head"]
+    gemm_ns = sum(sum(x) for x in tr["gemm"].values()) + tr["lm_head"]
+    n_gemm = 4 * L + 1
+    achieved = gemm_bytes / (gemm_ns * 1e-9) / 1e9
+    traffic = None
+    if args.layers <= 0:
+        traffic = round((L * sum(GEMM_TRAFFIC_MB[p] for p in PROJ) + GEMM_TRAFFIC_MB["lm_head"]) * 1e6 / n_gemm / 1e9, 5)
+    prof_gemm_ms = sum(prof[p][0] for p in ("qkv_gemm", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm"))
     step_ms = ms_max / args.steps
+    attn_launches = -(-S * 4 // 32)                   # query rows (heads x span rows) per launch: 32
+    launches_per_step = 3 + L * (4 + attn_launches) + 1 + 2
     out = {
         "metric": "committed tok/s (4B-shape verify, K=7, b1)",
         "value": round(committed_all / (ms_max * 1e-3), 3),
@@ -292,14 +349,25 @@ def run_ours(args, rank, world):
                    "mean_context": round(mean_ctx, 1), "graph": True, "pdl": True},
         "verify_hbm_gbs": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
         "step_roofline_frac": round(step_bytes / (step_ms * 1e-3) / 1e9 / peak, 4),
+        "step_bytes": int(step_bytes),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": dom_traffic,
-                     "traffic_unit": "GB per launch (ncu dram read + write)",
-                     "algorithmic": round(dom_bytes / max(dom_launches, 1) / 1e9, 5),
-                     "kernel": dom_name,
-                     "peak_kind": f"{peak_kind} (burst copy; each launch timed alone)",
-                     "launches": dom_launches, "avg_launch_us": round(dom_ms * 1e3 / max(dom_launches, 1), 2)},
-        "phases_ms_per_step": {p: round(prof[p][0] / args.steps, 4) for p in prof},
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "traffic_unit": "GB per launch (ncu dram read + write, 2-layer capture scaled by launch)",
+                     "algorithmic": round(gemm_bytes / n_gemm / 1e9, 5),
+                     "kernel": "gemm_kernel (tcgen05 weight-streaming GEMM, all projections + LM head)",
+                     "timing": ("in-graph: each launch's first CTA start to last CTA end (%globaltimer device "
+                                "timeline), summed over the 145 launches of the last of K traced steps"),
+                     "peak_kind": f"{peak_kind} (copy bandwidth)",
+                     "launches_per_step": n_gemm, "avg_launch_us": round(gemm_ns / n_gemm / 1e3, 2),
+                     "gemm_ms_per_step": round(gemm_ns / 1e6, 4),
+                     "traced_ms_per_step": round(traced_ms / args.steps, 4),
+                     "achieved_serialised": round(gemm_bytes * args.steps / (prof_gemm_ms * 1e-3) / 1e9, 1)},
+        "in_graph_us_per_layer": {
+            **{p: round(statistics.median(tr["gemm"][p]) / 1e3, 2) for p in PROJ},
+            "attention": round(statistics.median(tr["attention"]) / 1e3, 2),
+            "lm_head": round(tr["lm_head"] / 1e3, 2)},
+        "gemm_launch_phases_us": tr["gemm_detail_us"],
+        "phases_ms_per_step_serialised": {p: round(prof[p][0] / args.steps, 4) for p in prof},
         "e2e": {"value": round(e2e_committed_all / e2e_max, 3), "unit": "tok/s",
                 "h2d_bytes_per_step": K_DRAFT * 4, "d2h_bytes_per_step": (K_DRAFT + 2) * 4},
         "gpu_launches": launches_per_step * args.steps,
@@ -309,7 +377,7 @@ def run_ours(args, rank, world):
         "setup_s": round(setup_s, 1),
         "context_end": ctx_end,
     }
-    return out, host
+    return out
 
 
 # ----------------------------------------------------------------------------- further workloads
@@ -332,7 +400,7 @@ def _greedy_streams(v, loop, B, first_lens, steps):
     return streams
 
 
-def run_verify_workload(args, name, contexts, seed):
+def run_verify_workload(args, name, contexts, seed, dev, steps=None, warmup=None):
     """Verify steps over B sequences whose drafts are the target's own greedy continuation with
     each position replaced by a uniform token with probability 0.3 (mixed acceptance)."""
     import torch
@@ -340,11 +408,12 @@ def run_verify_workload(args, name, contexts, seed):
     from synth import workloads
     from speculative_decoding_verify_02_gb300 import SDV_DRAFT_TABLE, Verifier
     from speculative_decoding_verify_02_gb300.runner import SpecLoop
+    steps = steps or args.steps
+    warmup = warmup or args.warmup
     shape = synth.QWEN3_4B if args.layers <= 0 else synth.QWEN3_4B.with_layers(args.layers)
     t_setup = time.time()
-    host, dev = build_weights(shape, SEED)
     B = len(contexts)
-    gen_steps = (args.warmup + args.steps) * (K_DRAFT + 1) + 16
+    gen_steps = (warmup + steps) * (K_DRAFT + 1) + 16
     max_ctx = max(len(c) for c in contexts) + gen_steps + 64
     n_pages = sum(-(-(len(c) + gen_steps + 64) // 16) for c in contexts) + 8 * B
     v = Verifier(shape, dev, page_size=16, n_pages=n_pages, max_batch=B, max_rows=128, max_span=128,
@@ -361,7 +430,7 @@ def run_verify_workload(args, name, contexts, seed):
     loop.start([10_000_000] * B, k_init=K_DRAFT)
     kw = dict(drafter=SDV_DRAFT_TABLE, table=table, table_stride=table_len, ngram=False)
     loop.capture(**kw)
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         loop.replay()
     torch.cuda.synchronize()
     setup_s = time.time() - t_setup
@@ -376,45 +445,45 @@ def run_verify_workload(args, name, contexts, seed):
     clocks = ClockSampler(None)
     clocks.start()
     s = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(s)
-    for _ in range(args.steps):
-        loop.replay()
-    e1.record(s)
-    torch.cuda.synchronize()
+    ms = timed_replays(loop, steps, s)
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
     committed = total_len() - L0
     assert v.get_status() == 0
     v.profile_enable(True)  # per-phase device time (events around each launch group, eager steps)
     v.profile_read()
-    for _ in range(min(args.steps, 5)):
+    n_prof = min(steps, 5)
+    for _ in range(n_prof):
         loop.step(**kw)
     prof = v.profile_read()
     v.profile_enable(False)
-    n_prof = min(args.steps, 5)
+    v.close()
     mean_ctx = (L0 + L0 + committed) / 2 / B
-    step_ms = ms / args.steps
+    step_ms = ms / steps
     S = K_DRAFT + 1
     step_bytes = WEIGHT_BYTES_PER_STEP + B * (mean_ctx + S) * KV_BYTES_PER_TOKEN + B * S * EMBED_BYTES_PER_ROW
     peak, peak_kind = peaks()
     return {
         "metric": f"committed tok/s (4B-shape verify, K=7, {name})",
-        "value": round(committed / (ms * 1e-3), 3), "unit": "tok/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
-        "committed_per_step": round(committed / args.steps, 3),
+        "value": round(committed / (ms * 1e-3), 3), "unit": "tok/s", "n_gpus": 1, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "committed_per_step": round(committed / steps, 3),
         "dtype": "bf16", "data": "synthetic (seeded random-init weights and tokens)",
         "config": {"workload": name, "batch": B, "mean_context": round(mean_ctx, 1), "span": S,
                    "drafts": "greedy continuation, each position uniform-replaced with p=0.3", "graph": True},
         "verify_hbm_gbs": round(step_bytes / (step_ms * 1e-3) / 1e9, 1),
         "step_roofline_frac": round(step_bytes / (step_ms * 1e-3) / 1e9 / peak, 4),
         "step_bytes": int(step_bytes), "peak_kind": peak_kind, "clocks": clk, "setup_s": round(setup_s, 1),
-        "phases_ms_per_step": {p: round(prof[p][0] / n_prof, 4) for p in prof},
+        "phases_ms_per_step_serialised": {p: round(prof[p][0] / n_prof, 4) for p in prof},
     }
 
 
-def run_ngram_workload(args):
+def b16_contexts(vocab):
+    from synth import workloads
+    lens = workloads.context_lengths(3, 16)
+    return [workloads.uniform_context(3, int(n), vocab, name=f"b16.ctx.{b}") for b, n in enumerate(lens)]
+
+
+def run_ngram_workload(args, dev):
     """End-to-end n-gram speculation: 8 prompts of 1024 tokens (32-token spans, half repeating an
     earlier span), 256 greedy tokens each, 2-gram prompt lookup with adaptive K (start 1, +2 on a
     fully accepted round, -1 on any rejection, cap 7), against the same loop without drafts."""
@@ -424,7 +493,6 @@ def run_ngram_workload(args):
     from speculative_decoding_verify_02_gb300 import SDV_DRAFT_NGRAM, SDV_DRAFT_NONE, Verifier
     from speculative_decoding_verify_02_gb300.runner import SpecLoop
     shape = synth.QWEN3_4B
-    host, dev = build_weights(shape, SEED)
     B, GEN = 8, 256
     prompts = [workloads.span_repeat_prompt(5 + b, n_spans=32, span=32, vocab=shape.vocab) for b in range(B)]
     out = {}
@@ -459,6 +527,7 @@ def run_ngram_workload(args):
         gen = int(lens_t.sum().item()) - L0 + B      # + the first token of each sequence (from prefill)
         assert v.get_status() == 0
         out[mode] = {"tok_s": round(gen / (ms * 1e-3), 2), "ms": round(ms, 2), "steps": steps, "tokens": gen}
+        v.close()
         del v, loop
         torch.cuda.empty_cache()
     return {"metric": "committed tok/s, n-gram spec on vs off (4B shape, b8, 1024-token repeat-heavy prompts, 256 tokens)",
@@ -469,61 +538,104 @@ def run_ngram_workload(args):
 
 # ----------------------------------------------------------------------------- the oracle on the host cores
 
-def oracle_step_sample(host=None, n_layers_sample=1):
-    """Time the CPU oracle on a bounded sample of one S=8 verify step over an
-    848-token cache: n_layers_sample decoder layers plus the final norm and LM
-    head, with synthetic cache contents (timing only). The full step is
-    estimated as 36 x (time per layer) + (LM-head time)."""
+def _cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def oracle_verify_steps(n_steps, n_warmup):
+    """The CPU oracle, as it stands, on the headline workload: whole S=8 verify steps of the
+    36-layer 4B shape over an 848-token cache (synthetic cache contents; the weights are generated
+    before timing). Each step is timed alone. Returns (seconds per timed step, cores)."""
     import oracle
     import synth
     from synth import workloads
     shape = synth.QWEN3_4B
-    sample_shape = shape.with_layers(n_layers_sample)
-    if host is None:
-        host = {}
-
-    def get(n):
-        if n not in host:
-            host[n] = synth.tensor(shape, SEED, n)
-        return host[n]
-
-    model = oracle.DenseDecoder(sample_shape, get, cache_weights=False)
-    cache = oracle.SeqCache(sample_shape, CONTEXT + 16)
+    host = {n: synth.tensor(shape, SEED, n) for n in shape.tensor_shapes()}
+    model = oracle.DenseDecoder(shape, lambda n: host[n], cache_weights=False)
+    cache = oracle.SeqCache(shape, CONTEXT + 16)
     rng = np.random.default_rng(0)
-    for l in range(n_layers_sample):
+    for l in range(shape.n_layers):
         cache.K[l][:CONTEXT] = rng.standard_normal(cache.K[l][:CONTEXT].shape)
         cache.V[l][:CONTEXT] = rng.standard_normal(cache.V[l][:CONTEXT].shape)
-    cache.length = CONTEXT
     span = workloads.uniform_drafts(SEED, 0, K_DRAFT + 1, shape.vocab)
+    ts = []
+    for i in range(n_warmup + n_steps):
+        cache.length = CONTEXT
+        t0 = time.perf_counter()
+        model.forward([cache], [span])
+        if i >= n_warmup:
+            ts.append(time.perf_counter() - t0)
+    return ts, _cores()
+
+
+def oracle_tiny_generation():
+    """Config 1 end to end in the oracle: the tiny decoder, a 128-token motif prompt, 2-gram
+    drafts at fixed K = 4, 32 greedy tokens. Returns (seconds, committed tokens)."""
+    import oracle
+    import synth
+    from synth import workloads
+    shape = synth.TINY
+    host = {n: synth.tensor(shape, 1, n) for n in shape.tensor_shapes()}
+    model = oracle.DenseDecoder(shape, lambda n: host[n])
     t0 = time.perf_counter()
-    model.forward([cache], [span])
-    t_total = time.perf_counter() - t0
-    # split the sample into layer time and head time
-    y = np.zeros((K_DRAFT + 1, shape.hidden))
-    t1 = time.perf_counter()
-    oracle.rmsnorm(y, model.w("final_norm"), shape.rms_eps) @ model.w("lm_head").T
-    t_head = time.perf_counter() - t1
-    t_layer = max(t_total - t_head, 1e-6) / n_layers_sample
-    t_step = shape.n_layers * t_layer + t_head
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return t_step, t_total + t_head, cores
+    streams, _, _ = oracle.generate(model, [workloads.motif_prompt(1)], 32, drafter="ngram", k=4)
+    return time.perf_counter() - t0, len(streams[0])
+
+
+def cpu_child(kind):
+    """Entry of the child process that times the oracle (a fresh interpreter: no CUDA context,
+    no torch thread pools competing with the BLAS threads)."""
+    if kind == "verify":
+        ts, cores = oracle_verify_steps(1, 0)
+        print(json.dumps({"step_s": ts[0], "cores": cores}))
+    elif kind == "tiny":
+        s, n = oracle_tiny_generation()
+        print(json.dumps({"seconds": s, "tokens": n, "cores": int(os.environ.get("OPENBLAS_NUM_THREADS", _cores()))}))
+
+
+def spawn_cpu_child(kind, threads=None, timeout=900):
+    env = dict(os.environ)
+    if threads is not None:
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            env[k] = str(threads)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", kind], env=env,
+                       capture_output=True, text=True, timeout=timeout)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else f"rc {r.returncode}"}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline():
+    """The oracle timed on the host cores, each figure in a fresh process."""
+    step = spawn_cpu_child("verify")
+    tiny_all = spawn_cpu_child("tiny")
+    tiny_one = spawn_cpu_child("tiny", threads=1)
+    out = {"unit": "tok/s", "kind": "oracle"}
+    if "step_s" in step:
+        out.update({"value": round(1.0 / step["step_s"], 6), "cores": step["cores"],
+                    "sample": (f"one whole S=8 verify step of the 36-layer 4B shape over an 848-token cache "
+                               f"(1 committed token at uniform drafts), timed alone in a fresh process: "
+                               f"{step['step_s']:.2f} s; BLAS on {step['cores']} threads, the oracle's "
+                               f"bf16-to-float64 weight conversion on one")})
+    else:
+        out.update({"value": None, "cores": _cores(), "sample": f"oracle step failed: {step['error']}"})
+    if "seconds" in tiny_all and "seconds" in tiny_one:
+        out["tiny_config_e2e"] = {"workload": "tiny decoder, 128-token motif prompt, 2-gram K=4, 32 tokens",
+                                  "s_all_threads": round(tiny_all["seconds"], 3), "threads": tiny_all["cores"],
+                                  "s_one_thread": round(tiny_one["seconds"], 3)}
+    return out
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the CPU oracle, as it stands, on the same workload."""
+    """The reference arm: the CPU oracle, as it stands, on the headline workload, W warm-up and K
+    timed whole verify steps (36 layers, S = 8) on the host cores."""
     if rank != 0:
         return None
-    import synth
-    ts = []
-    host = {}
-    for i in range(args.warmup + args.steps):
-        t_step, _, cores = oracle_step_sample(host)
-        if i >= args.warmup:
-            ts.append(t_step)
+    ts, cores = oracle_verify_steps(args.steps, args.warmup)
     mean = sum(ts) / len(ts)
     value = 1.0 / mean               # uniform drafts: one committed token per verify step
-    sample = (f"per step: one S=8 verify of the 4B shape over an 848-token cache, 1 decoder layer + final norm "
-              f"+ LM head computed, full step = 36 x layer + head")
+    sample = (f"per step: one whole S=8 verify of the 36-layer 4B shape over an 848-token cache, each step "
+              f"timed alone (min {min(ts):.2f} s, max {max(ts):.2f} s)")
     return {
         "impl": "reference",
         "metric": "committed tok/s (4B-shape verify, K=7, b1)",
@@ -545,53 +657,66 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-extra", dest="extra", action="store_false",
+                    help="skip the batch-16 and 32K-context sub-objects of the headline line")
     ap.add_argument("--workload", default="b1", choices=["b1", "b16", "ctx32k", "ngram"],
                     help="b1 (default, the headline line): batch 1, 848-token context; b16: 16 sequences with "
                          "contexts U[512, 4096]; ctx32k: batch 1, 32768-token context; ngram: end-to-end 2-gram "
                          "speculation against the same loop without drafts")
     ap.add_argument("--layers", type=int, default=0,
                     help="decoder layers (default: all 36); fewer only for small profiling cases")
+    ap.add_argument("--cpu-child", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_child:
+        cpu_child(args.cpu_child)
+        return
     args.warmup = max(args.warmup, 3)
     rank, local, world = dist_env()
 
     if args.impl == "reference":
-        if world > 1:
-            import torch.distributed as dist
-            dist.init_process_group("gloo")
         out = run_reference(args, rank, world)
         if rank == 0:
             print(json.dumps(out), flush=True)
         return
 
     import torch
+    import synth
+    torch.cuda.set_device(local)
+    shape = synth.QWEN3_4B if args.layers <= 0 else synth.QWEN3_4B.with_layers(args.layers)
     if args.workload != "b1":
         if rank == 0:  # single-GPU measurement lines for the other workloads
-            import synth
             from synth import workloads
-            vocab = synth.QWEN3_4B.vocab
+            dev = build_weights(shape, SEED)
             if args.workload == "b16":
-                lens = workloads.context_lengths(3, 16)
-                ctxs = [workloads.uniform_context(3, int(n), vocab, name=f"b16.ctx.{b}") for b, n in enumerate(lens)]
-                out = run_verify_workload(args, "qwen3-4b-shape verify, batch 16, contexts U[512, 4096], K=7", ctxs, 3)
+                out = run_verify_workload(args, "qwen3-4b-shape verify, batch 16, contexts U[512, 4096], K=7",
+                                          b16_contexts(shape.vocab), 3, dev)
             elif args.workload == "ctx32k":
-                ctxs = [workloads.uniform_context(4, 32768, vocab)]
-                out = run_verify_workload(args, "qwen3-4b-shape verify, batch 1, 32768-token context, K=7", ctxs, 4)
+                out = run_verify_workload(args, "qwen3-4b-shape verify, batch 1, 32768-token context, K=7",
+                                          [workloads.uniform_context(4, 32768, shape.vocab)], 4, dev)
             else:
-                out = run_ngram_workload(args)
+                out = run_ngram_workload(args, dev)
             print(json.dumps(out), flush=True)
         return
     if world > 1:
-        torch.cuda.set_device(local)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    out, host = run_ours(args, rank, world)
+    dev = build_weights(shape, SEED)
+    out = run_ours(args, rank, world, dev)
+    if rank == 0 and world == 1 and args.extra:
+        from synth import workloads
+        steps, warm = min(args.steps, 20), 3
+        for key, name, ctxs, seed in (
+                ("b16", "qwen3-4b-shape verify, batch 16, contexts U[512, 4096], K=7", b16_contexts(shape.vocab), 3),
+                ("ctx32k", "qwen3-4b-shape verify, batch 1, 32768-token context, K=7",
+                 [workloads.uniform_context(4, 32768, shape.vocab)], 4)):
+            r = run_verify_workload(args, name, ctxs, seed, dev, steps=steps, warmup=warm)
+            out[key] = {k: r[k] for k in ("value", "unit", "ms_per_step", "committed_per_step", "steps", "warmup",
+                                          "verify_hbm_gbs", "step_roofline_frac", "step_bytes", "clocks")}
+            out[key]["config"] = r["config"]
+            out[key]["phases_ms_per_step_serialised"] = r["phases_ms_per_step_serialised"]
+            torch.cuda.empty_cache()
     if rank == 0:
         if args.cpu_baseline and world == 1:
-            t_step, spent, cores = oracle_step_sample(host)
-            out["cpu_baseline"] = {"value": round(1.0 / t_step, 6), "unit": "tok/s", "cores": cores, "kind": "oracle",
-                                   "sample": (f"one S=8 verify of the 4B shape over an 848-token cache: 1 decoder "
-                                              f"layer + final norm + LM head computed in {spent:.1f} s, full step "
-                                              f"estimated as 36 x layer + head = {t_step:.1f} s")}
+            out["cpu_baseline"] = cpu_baseline()
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.barrier()

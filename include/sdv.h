@@ -281,19 +281,30 @@ int sdv_fwd_trace(sdv_ctx *ctx, void *d_buf, size_t bytes);
  *   Scratch: a file-scope device array of 8 MiB, held by every GPU that loads
  *   the library until the process exits. The first call on a device resolves
  *   that array's device address and sets kernel attributes; make that first
- *   call before any stream capture. All calls share the array, so calls that
- *   overlap on the GPU race (calls on different devices do not share it); group counters are cleared on every call.
+ *   call before any stream capture. The resolved address is kept for the life
+ *   of the process: calls on a device after cudaDeviceReset are not
+ *   supported. All calls share the array, so calls that overlap on the GPU
+ *   race (calls on different devices do not share it); each call clears the
+ *   status word and the group counters it uses.
  *   Limits: B <= 64, head_dim 64 or 128, every L_b + S_b <= max_context <=
  *   pages_per_seq * page_size, and the scratch the shapes need (about
- *   B * ceil(max_context/1024) * n_kv_heads * n_q_heads/n_kv_heads *
- *   min(max_span, 128*n_kv_heads/n_q_heads) * (4*head_dim + 8) bytes) within
- *   8 MiB; beyond it the call returns SDV_ERR_CAPACITY and enqueues nothing.
- *   A sequence whose span passes max_context gets NaN rows. No device memory
- *   is allocated or freed. */
+ *   B * ceil(max_context/1024) * n_q_heads * min(max_span,
+ *   64*n_kv_heads/n_q_heads) * (4*head_dim + 8) bytes) within 8 MiB; beyond it
+ *   the call returns SDV_ERR_CAPACITY and enqueues nothing.
+ *   Device-side errors go to a status word in the scratch, read with
+ *   sdv_noalloc_status: a sequence whose span is longer than max_span
+ *   (SDV_ERR_ARG) or passes max_context (SDV_ERR_CAPACITY) gets NaN rows; a
+ *   page id outside [0, n_pages) reads as zero K/V rows and sets
+ *   SDV_ERR_CAPACITY. No device memory is allocated or freed. */
 int sdv_paged_attention_noalloc(const void *d_q, const void *d_kv_layer, const int32_t *d_page_table,
                                 int pages_per_seq, int page_size, int n_pages, const int32_t *d_row_off,
                                 const int32_t *d_base, int B, int n_q_heads, int n_kv_heads, int head_dim,
                                 int max_span, int max_context, void *d_out, void *stream);
+
+/* Synchronise the current device, copy the status word of the last
+ * sdv_paged_attention_noalloc call on it to *h_status (SDV_OK if none ran) and
+ * clear it. Allocates nothing. The pages have no counterpart of this call. */
+int sdv_noalloc_status(int32_t *h_status);
 
 #ifdef __cplusplus
 }

@@ -31,7 +31,7 @@ EXPORTS = (
     "sdv_spec_forward", "sdv_accept_greedy", "sdv_rewind_cache", "sdv_cache_seq_len", "sdv_page_table",
     "sdv_ngram_commit", "sdv_gen_init", "sdv_propose", "sdv_reset_seq", "sdv_get_status", "sdv_status_str",
     "sdv_op_attention", "sdv_profile_enable", "sdv_profile_read", "sdv_paged_attention_noalloc",
-    "sdv_fwd_trace",
+    "sdv_fwd_trace", "sdv_noalloc_status",
 )
 PHASES = ("prepare", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm")
 # sdv_fwd_trace: stamps per CTA, CTAs per region (one region per launch of a forward)
@@ -104,6 +104,7 @@ def lib():
     L.sdv_profile_read.argtypes = [vp, P(ctypes.c_float), P(ctypes.c_int32)]
     L.sdv_fwd_trace.argtypes = [vp, vp, ctypes.c_size_t]
     L.sdv_paged_attention_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+    L.sdv_noalloc_status.argtypes = [P(ctypes.c_int32)]
     for name in EXPORTS:
         if name != "sdv_status_str":
             getattr(L, name).restype = i32
@@ -154,6 +155,14 @@ def paged_attention_noalloc(q, kv_layer, page_table, pages_per_seq, page_size, n
                                              n_pages, _ptr(row_off), _ptr(base), B, n_q_heads, n_kv_heads, head_dim,
                                              max_span, max_context, _ptr(out), _stream(stream)),
            "paged_attention_noalloc")
+
+
+def noalloc_status() -> int:
+    """Status word of the last paged_attention_noalloc call on the current device (synchronises,
+    then clears it)."""
+    v = ctypes.c_int32()
+    _check(lib().sdv_noalloc_status(ctypes.byref(v)), "noalloc_status")
+    return v.value
 
 
 def upload_bf16(bits: np.ndarray, device="cuda"):

@@ -54,20 +54,27 @@ Layout layout(int B, int nkv, int D, int rows_per_item, int max_work) {
     return L;
 }
 
-// One block: the work list (one item per 1024-position group of every sequence
-// with a span), zeroed group counters, and NaN rows for any sequence whose
-// span passes max_context (it gets no work).
-__global__ void noalloc_prep_kernel(const int *row_off, const int *base, int B, int nkv, int max_context, int max_work,
-                                    int *status, int *n_work, int4 *work, int *counters, bf16 *out, int row_elems) {
+// One block: clears the status word, builds the work list (one item per 1024-position group of
+// every accepted sequence with a span), zeroes the group counters, and writes NaN rows for every
+// sequence it rejects: a span longer than max_span (SDV_ERR_ARG) or one that passes max_context
+// (SDV_ERR_CAPACITY) gets no work, so its rows would otherwise keep stale memory.
+__global__ void noalloc_prep_kernel(const int *row_off, const int *base, int B, int nkv, int max_span,
+                                    int max_context, int max_work, int *status, int *n_work, int4 *work,
+                                    int *counters, bf16 *out, int row_elems) {
     pdl_wait();
     __shared__ int off_s[65];
     for (int i = threadIdx.x; i < B * nkv * kAttnCluster; i += blockDim.x) counters[i] = 0;
     if (threadIdx.x == 0) {
+        *status = 0;
         int nw = 0;
         for (int b = 0; b < B; ++b) {
             const int S = row_off[b + 1] - row_off[b], L = base[b];
             off_s[b] = nw;
-            if (S <= 0) continue;
+            if (S == 0) continue;
+            if (S < 0 || S > max_span) {
+                set_status(status, SDV_ERR_ARG);
+                continue;
+            }
             if (L < 0 || L + S > max_context) {
                 set_status(status, SDV_ERR_CAPACITY);
                 continue;
@@ -165,8 +172,8 @@ extern "C" int sdv_paged_attention_noalloc(const void *d_q, const void *d_kv_lay
     int *n_work = status + 1;
     int4 *work = reinterpret_cast<int4 *>(scratch + L.work);
     int *counters = reinterpret_cast<int *>(scratch + L.counters);
-    noalloc_prep_kernel<<<1, 256, 0, st>>>(d_row_off, d_base, B, n_kv_heads, max_context, max_work, status, n_work,
-                                            work, counters, static_cast<bf16 *>(d_out), n_q_heads * head_dim);
+    noalloc_prep_kernel<<<1, 256, 0, st>>>(d_row_off, d_base, B, n_kv_heads, max_span, max_context, max_work, status,
+                                            n_work, work, counters, static_cast<bf16 *>(d_out), n_q_heads * head_dim);
     if (cudaGetLastError() != cudaSuccess) return SDV_ERR_CUDA;
 
     AttnArgs a{};
@@ -197,5 +204,27 @@ extern "C" int sdv_paged_attention_noalloc(const void *d_q, const void *d_kv_lay
                                               : launch_attn<64>(a, max_work, n_kv_heads, st);
         if (e != cudaSuccess) return SDV_ERR_CUDA;
     }
+    return SDV_OK;
+}
+
+extern "C" int sdv_noalloc_status(int32_t *h_status) {
+    if (!h_status) return SDV_ERR_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SDV_ERR_CUDA;
+    unsigned char *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mu);
+        if (g_setup[dev].done) scratch = g_setup[dev].scratch;
+    }
+    if (!scratch) {  // no call has run on this device: nothing to report
+        *h_status = SDV_OK;
+        return SDV_OK;
+    }
+    if (cudaDeviceSynchronize() != cudaSuccess) return SDV_ERR_CUDA;
+    int v = 0;
+    const int zero = 0;
+    if (cudaMemcpy(&v, scratch, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SDV_ERR_CUDA;
+    if (cudaMemcpy(scratch, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return SDV_ERR_CUDA;
+    *h_status = v;
     return SDV_OK;
 }

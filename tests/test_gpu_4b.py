@@ -11,7 +11,7 @@ import pytest
 import oracle
 import synth
 from synth import workloads
-from tests.helpers import MARGIN, check_rows, margins, upload_weights
+from tests.helpers import MARGIN, check_rows, margins, oracle_cache_from_pool, upload_weights
 
 pytestmark = pytest.mark.gpu
 
@@ -164,3 +164,36 @@ def test_batch16_ragged_teacher_forced(model):
     assert len(set(ms)) >= 3, ms                               # mixed acceptance lengths were exercised
     print(f"batch16: {checked} sequence-steps compared exactly, near-tie flips {flips_all}, m histogram "
           f"{np.bincount(ms).tolist()}")
+
+
+def test_verify_every_span_length_1_to_17(model):
+    """[CA] verify cost against S: the config-2 sweep S = 1..17 at an 848-token context. Every
+    span is checked against the oracle's verify over the same (GPU-written) context, and its rows
+    must equal the first rows of the 17-row span bit for bit (one-row to 17-row forwards, GEMM
+    widths 16 and 32, one to three attention launches)."""
+    host, dev, om = model
+    ctx = workloads.uniform_context(SEED, 848, SHAPE.vocab, name="sweep.ctx")
+    toks = [int(t) for t in synth.tokens(SEED, "sweep.span", 17, SHAPE.vocab)]
+    from speculative_decoding_verify_02_gb300.runner import SpecLoop
+    v = _verifier(dev)
+    SpecLoop(v, 1, 17).prefill([ctx])
+    base = oracle_cache_from_pool(v, SHAPE, 0, 848, 900)
+    wide, worst, flips_all = None, 0.0, []
+    for S in [17] + list(range(1, 17)):
+        v.ensure_capacity(_t([848 + 17]), 1)
+        lg, am = _forward(v, toks[:S], [0, S], 1, S)
+        v.rewind_cache(_t([848]), 1)
+        assert v.get_status() == 0
+        cache = oracle.SeqCache(SHAPE, 900, kv_dtype="bf16")
+        for l in range(SHAPE.n_layers):
+            cache.K[l][:848], cache.V[l][:848] = base.K[l][:848], base.V[l][:848]
+        cache.length = 848
+        ref = om.forward([cache], [toks[:S]])[0]
+        flips, d = check_rows(lg, am, ref, f"sweep S={S}")
+        worst = max(worst, d)
+        flips_all += [(S, f) for f in flips]
+        if wide is None:
+            wide = lg
+        else:
+            assert np.abs(lg - wide[:S]).max() == 0.0, (S, np.abs(lg - wide[:S]).max())
+    print(f"sweep S=1..17: max |dlogit| {worst:.3e}, near-tie flips {flips_all}")

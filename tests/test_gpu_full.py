@@ -12,6 +12,11 @@ from tests.helpers import MARGIN, check_rows, margins
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
+# Bound on max |dlogit| of the 36-layer verify against the oracle whose cache keeps K/V in float64
+# instead of bf16: the K/V rounding alone moves logits by about 0.02 per 2 layers of emulation and
+# measured 0.054 at 36 layers; the bar is set at 0.1.
+EXACT_KV_BOUND = 0.1
+
 
 def _t(a):
     import torch
@@ -44,19 +49,28 @@ def test_full_model_verify_step_848():
     torch.cuda.synchronize()
     assert v.get_status() == 0
     flips, d = check_rows(lg.cpu().numpy(), am.cpu().numpy(), ref, "36-layer verify")
-    # for information: the same step against an oracle whose cache keeps K/V exactly
+    # The same step against an oracle whose cache keeps K/V exactly (the literal fp32 reading of the
+    # bar): the bf16 K/V storage costs up to EXACT_KV_BOUND on the logits at 36 layers, and every row
+    # whose exact-KV top-2 margin exceeds twice the measured difference keeps its argmax.
     exact = oracle.SeqCache(shape, 900)
     om.forward([exact], [ctx], last_row_logits=True)
     ref64 = om.forward([exact], [span])[0]
-    d64 = float(np.abs(lg.cpu().numpy().astype(np.float64) - ref64).max())
-    print(f"36-layer verify at 848: max |dlogit| {d:.3e} (bf16 KV oracle), {d64:.3e} (exact-KV oracle), "
-          f"near-tie flips {flips}")
+    g = lg.cpu().numpy().astype(np.float64)
+    d64 = float(np.abs(g - ref64).max())
+    assert d64 <= EXACT_KV_BOUND, f"exact-KV oracle: max |dlogit| {d64:.4g} > {EXACT_KV_BOUND}"
+    sure = margins(ref64) > 2 * d64
+    np.testing.assert_array_equal(am.cpu().numpy()[sure], ref64.argmax(-1)[sure])
+    print(f"36-layer verify at 848: max |dlogit| {d:.3e} (bf16 KV oracle), {d64:.3e} (exact-KV oracle, "
+          f"{int(sure.sum())}/8 rows argmax-checked), near-tie flips {flips}")
 
 
-def test_attention_32k_context():
-    """Paged attention of an 8-row span over a 32768-token cache (33 key groups
-    of 1024 positions)."""
-    attention_long_context(32768, 8)
+@pytest.mark.parametrize("L,S", [(32768, 8), (1020, 8), (2040, 16)])
+def test_attention_long_context(L, S):
+    """Paged attention of an S-row span over an L-token cache: 32768 + 8 (33 key groups of 1024
+    positions), and spans straddling a key group (1020 + 8, 2040 + 16), whose first rows see no
+    key of the last group, so that group's state is empty for them and must contribute nothing to
+    the merge across groups; 2040 + 16 also takes two launches of 8 span rows."""
+    attention_long_context(L, S)
 
 
 def attention_long_context(L, S):

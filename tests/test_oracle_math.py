@@ -261,3 +261,26 @@ def test_bf16_kv_cache_stores_rounded_values(tiny):
     for l in range(synth.TINY.n_layers):                       # every stored value is a bf16 value
         np.testing.assert_array_equal(b.K[l][:12], round_bf16(b.K[l][:12]))
         np.testing.assert_array_equal(b.V[l][:12], round_bf16(b.V[l][:12]))
+
+
+def test_argmax_lowest_index_wins_exact_ties():
+    """The tie rule of the per-row argmax: among exactly equal maxima the lowest
+    vocabulary index is reported. Hand-made rows put the tie at the front, the
+    back, far apart and across the whole row; random rows over a three-value
+    alphabet (ties everywhere) are checked against the first index holding the
+    row maximum, found by a plain scan."""
+    from oracle import argmax_lowest
+    rows = np.array([
+        [5.0, 3.0, 5.0, 1.0, 5.0],      # tie at 0, 2, 4 -> 0
+        [1.0, 7.0, 2.0, 7.0, 0.0],      # tie at 1, 3 -> 1
+        [0.0, 0.0, 0.0, 0.0, 9.0],      # unique maximum at the end -> 4
+        [-1.0, -2.0, -3.0, 4.0, 4.0],   # tie at the last two -> 3
+        [2.5, 2.5, 2.5, 2.5, 2.5],      # all equal -> 0
+        [-np.inf, -7.0, -np.inf, -7.0, -8.0],
+    ])
+    np.testing.assert_array_equal(argmax_lowest(rows), [0, 1, 4, 3, 0, 1])
+    r = np.random.default_rng(7).integers(0, 3, size=(400, 37)).astype(np.float64)
+    expect = [next(i for i in range(r.shape[1]) if r[k, i] == r[k].max()) for k in range(r.shape[0])]
+    np.testing.assert_array_equal(argmax_lowest(r), expect)
+    # a batch of logits [B, S, V] reduces over the last axis only
+    np.testing.assert_array_equal(argmax_lowest(rows.reshape(2, 3, 5)), [[0, 1, 4], [3, 0, 1]])
