@@ -154,6 +154,28 @@ int sdv_ensure_capacity(sdv_ctx *ctx, const int32_t *d_required, int B, void *st
 int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row_off, int B, int max_rows,
                      int max_span, int32_t *d_argmax, float *d_logits, void *stream);
 
+/* [TS] the protocol, Verify: "the caller's sampler draws each row and drafts
+ * are accepted while the drawn token matches".
+ * The same forward as sdv_spec_forward, with each row drawn from
+ * softmax(logits / T_b) instead of taking its argmax: row r of sequence b at
+ * position p draws argmax_v(logit_v / T_b + g_v), g_v = -log(-log u_v) (the
+ * Gumbel-max construction), in float32. u_v comes from SplitMix64 streams
+ * (Steele, Lea and Flood 2014; stream(k)[i] = mix64(k + (i+1) *
+ * 0x9E3779B97F4A7C15)): x = stream(stream(stream(seed)[b])[p])[v],
+ * u = ((x >> 41) + 1/2) * 2^-23. The noise of a position depends only on
+ * (seed, b, p, v), so with a fixed seed a position draws the same token
+ * whether it is verified in a span or decoded alone, and sdv_accept_greedy
+ * on the drawn tokens is the sampled accept rule (speculation stays lossless).
+ *   d_temperature [B] float (device): T_b; T_b <= 0 draws the argmax (greedy).
+ *   seed          the generation's key; keep it fixed across a generation.
+ *   d_drawn       [R] int32 out: the drawn token of each row.
+ *   d_logits      as in sdv_spec_forward (the unperturbed logits), or NULL.
+ * Other arguments, errors and effects as sdv_spec_forward; a NULL
+ * d_temperature returns SDV_ERR_ARG. */
+int sdv_spec_forward_sampled(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row_off, int B, int max_rows,
+                             int max_span, const float *d_temperature, uint64_t seed, int32_t *d_drawn,
+                             float *d_logits, void *stream);
+
 /* [PI] the transaction, Accept; draft-seed alignment; [TS] the protocol.
  * For each sequence with S_b = k+1 >= 1 rows (drafts d_1..d_k = span rows
  * 1..k, argmax a_0..a_k): m_b = the largest j <= k with d_i == a_{i-1} for

@@ -31,8 +31,10 @@ from .model import DenseDecoder, SeqCache, rmsnorm, silu, rope_neox, attention_r
 from .pages import PagePool, CapacityError
 from .spec import accept_greedy, ngram_propose, adapt_k
 from .loop import generate, StepRecord
+from .sampling import draw_rows, perturbed, gumbel, uniforms
 
 __all__ = [
     "DenseDecoder", "SeqCache", "round_bf16", "rmsnorm", "silu", "rope_neox", "attention_rows", "argmax_lowest",
     "PagePool", "CapacityError", "accept_greedy", "ngram_propose", "adapt_k", "generate", "StepRecord",
+    "draw_rows", "perturbed", "gumbel", "uniforms",
 ]

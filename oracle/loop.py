@@ -12,6 +12,8 @@ batch of sequences. TEST INFRASTRUCTURE.
   [PI] losslessness / [CA] "off is the identical loop with drafting disabled":
        the plain loop is this loop with no drafts (one-row steps).
   [CA] "adaptive K".
+  [TS] "the protocol", Verify: the caller's sampler draws each row and drafts
+       are accepted while the drawn token matches (oracle.sampling).
 
 Conventions (readings): the prompt is prefilled sequence by sequence in
 chunks of at most ``prefill_chunk`` tokens, each chunk preceded by a capacity
@@ -27,6 +29,7 @@ import numpy as np
 
 from .model import SeqCache, argmax_lowest
 from .pages import PagePool
+from .sampling import draw_rows
 from .spec import accept_greedy, adapt_k, ngram_propose
 
 
@@ -46,12 +49,14 @@ class StepRecord:
 def generate(model, prompts, n_tokens: int, drafter: str = "ngram", k: int = 4, adaptive: bool = False,
              k_max: int = 7, ngram_n: int = 2, tables=None, page_size: int = 16, n_pages: int = None,
              max_pages_per_seq: int = None, prefill_chunk: int = 128, keep_logits: bool = False,
-             kv_dtype: str = "f64"):
+             kv_dtype: str = "f64", temperature: float = 0.0, seed: int = 0):
     """Run the loop for every sequence until each has n_tokens generated tokens.
 
     drafter: "ngram" (prompt lookup over the sequence's history), "table"
     (drafts = tables[b][g : g+k] where g tokens are generated so far), or
-    "none" (the plain loop: one-row steps). Returns (streams, records, pool).
+    "none" (the plain loop: one-row steps). temperature > 0 draws every row
+    with the sampler of oracle.sampling (key `seed`, sequence slot b, the row's
+    position) instead of taking its argmax. Returns (streams, records, pool).
     """
     sh = model.shape
     B = len(prompts)
@@ -62,6 +67,11 @@ def generate(model, prompts, n_tokens: int, drafter: str = "ngram", k: int = 4, 
         n_pages = B * max_pages_per_seq
     caches = [SeqCache(sh, cap, kv_dtype) for _ in range(B)]
     pool = PagePool(n_pages, page_size, B, max_pages_per_seq)
+
+    def draw(b, logits, positions):
+        if temperature > 0:
+            return [int(x) for x in draw_rows(logits, temperature, seed, b, positions)]
+        return [int(x) for x in argmax_lowest(logits)]
 
     last_logits = []
     for b in range(B):                                        # prefill, sequence by sequence
@@ -77,7 +87,7 @@ def generate(model, prompts, n_tokens: int, drafter: str = "ngram", k: int = 4, 
             lg = model.forward(caches, spans, last_row_logits=True)[b]
             pool.set_length(b, caches[b].length)
         last_logits.append(lg[-1])
-    first = [int(argmax_lowest(v)) for v in last_logits]
+    first = [draw(b, last_logits[b][None], [len(prompts[b]) - 1])[0] for b in range(B)]
     streams = [[f] for f in first]
     hists = [list(map(int, prompts[b])) + [first[b]] for b in range(B)]
     K = [1 if adaptive else k for _ in range(B)]
@@ -114,7 +124,7 @@ def generate(model, prompts, n_tokens: int, drafter: str = "ngram", k: int = 4, 
             if not active[b]:
                 am.append([]); ms.append(-1); com.append([]); new_len.append(-1)
                 continue
-            a = [int(x) for x in argmax_lowest(lg[b])]
+            a = draw(b, lg[b], [len_before[b] + i for i in range(len(spans[b]))])
             m, c = accept_greedy(drafts[b], a)
             am.append(a); ms.append(m); com.append(c)
             new_len.append(len_before[b] + m + 1)

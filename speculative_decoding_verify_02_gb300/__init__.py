@@ -28,7 +28,7 @@ SDV_DRAFT_NONE, SDV_DRAFT_NGRAM, SDV_DRAFT_TABLE = 0, 1, 2
 # Every entry point include/sdv.h declares.
 EXPORTS = (
     "sdv_workspace_bytes", "sdv_kv_pool_bytes", "sdv_create", "sdv_destroy", "sdv_ensure_capacity",
-    "sdv_spec_forward", "sdv_accept_greedy", "sdv_rewind_cache", "sdv_cache_seq_len", "sdv_page_table",
+    "sdv_spec_forward", "sdv_spec_forward_sampled", "sdv_accept_greedy", "sdv_rewind_cache", "sdv_cache_seq_len", "sdv_page_table",
     "sdv_ngram_commit", "sdv_gen_init", "sdv_propose", "sdv_reset_seq", "sdv_get_status", "sdv_status_str",
     "sdv_op_attention", "sdv_profile_enable", "sdv_profile_read", "sdv_paged_attention_noalloc",
     "sdv_fwd_trace", "sdv_noalloc_status",
@@ -88,6 +88,7 @@ def lib():
     L.sdv_destroy.argtypes = [vp]
     L.sdv_ensure_capacity.argtypes = [vp, vp, i32, vp]
     L.sdv_spec_forward.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
+    L.sdv_spec_forward_sampled.argtypes = [vp, vp, vp, i32, i32, i32, vp, ctypes.c_uint64, vp, vp, vp]
     L.sdv_accept_greedy.argtypes = [vp, vp, vp, vp, i32, i32, vp, vp, vp, vp, vp]
     L.sdv_rewind_cache.argtypes = [vp, vp, i32, vp]
     L.sdv_cache_seq_len.argtypes = [vp, vp, vp]
@@ -217,6 +218,15 @@ class Verifier:
     def spec_forward(self, tokens, row_off, B, max_rows, max_span, argmax, logits=None, stream=None):
         _check(lib().sdv_spec_forward(self.ctx, _ptr(tokens), _ptr(row_off), B, max_rows, max_span, _ptr(argmax),
                                       _ptr(logits), _stream(stream)), "spec_forward")
+
+    def spec_forward_sampled(self, tokens, row_off, B, max_rows, max_span, temperature, seed, drawn, logits=None,
+                             stream=None):
+        """The verify forward with each row drawn at its sequence's temperature (float32 device
+        tensor [B]; <= 0 = greedy) from the noise keyed by `seed`, the sequence slot and the row's
+        position."""
+        _check(lib().sdv_spec_forward_sampled(self.ctx, _ptr(tokens), _ptr(row_off), B, max_rows, max_span,
+                                              _ptr(temperature), int(seed) & (2**64 - 1), _ptr(drawn),
+                                              _ptr(logits), _stream(stream)), "spec_forward_sampled")
 
     def accept_greedy(self, tokens, row_off, argmax, B, max_commit, n_accept, committed, n_commit, new_len,
                       stream=None):

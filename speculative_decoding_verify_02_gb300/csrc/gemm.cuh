@@ -59,6 +59,10 @@ struct GemmArgs {
     float *logits;
     int *argmax_out, *done_counter;
     int vocab;
+    // sampled verify: per-sequence temperatures ([max_batch], <= 0 = greedy) or nullptr, and the
+    // key of the row noise (the rows' sequences and positions come from row_seq / row_pos)
+    const float *temperature;
+    unsigned long long seed;
     unsigned long long *trace;         // optional timeline: 16 %globaltimer stamps per CTA, or nullptr
 };
 
@@ -319,8 +323,38 @@ __device__ __forceinline__ void epi_swiglu_row(const GemmArgs &a, float rstd, in
     }
 }
 
+// SplitMix64 (Steele, Lea and Flood, OOPSLA 2014): the output function, and output i of the
+// stream keyed k, mix64(k + (i + 1) * golden gamma).
+__device__ __forceinline__ unsigned long long splitmix_mix(unsigned long long z) {
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+__device__ __forceinline__ unsigned long long splitmix_at(unsigned long long k, unsigned long long i) {
+    return splitmix_mix(k + (i + 1ull) * 0x9E3779B97F4A7C15ull);
+}
+
+// Gumbel noise of vocabulary entry v in the stream of one row: u = ((x >> 41) + 1/2) 2^-23 is a
+// 23-bit uniform strictly inside (0, 1) that float32 holds exactly; g = -log(-log u).
+__device__ __forceinline__ float row_gumbel(unsigned long long row_key, int v) {
+    const unsigned long long xr = splitmix_at(row_key, static_cast<unsigned long long>(v));
+    const float u = (static_cast<float>(xr >> 41) + 0.5f) * 1.1920928955078125e-07f;
+    return -logf(-logf(u));
+}
+
 __device__ __forceinline__ void epi_lmhead_row(const GemmArgs &a, float rstd, int tile, int r, int lane,
                                                float (&x)[4]) {
+    // sampled rows: the argmax of logit / T + g(seed, sequence, position, v) (Gumbel-max draw)
+    float T = 0.f;
+    unsigned long long rkey = 0;
+    if (a.temperature != nullptr) {
+        const int seq = a.row_seq[r];
+        T = seq >= 0 ? a.temperature[seq] : 0.f;
+        if (T > 0.f) {
+            rkey = splitmix_at(splitmix_at(a.seed, static_cast<unsigned long long>(seq)),
+                               static_cast<unsigned long long>(a.row_pos[r]));
+        }
+    }
     uint32_t best = 0, bidx = 0xffffffffu;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {  // ascending vocabulary index: the first maximum is the lowest index
@@ -328,7 +362,8 @@ __device__ __forceinline__ void epi_lmhead_row(const GemmArgs &a, float rstd, in
         if (v < a.vocab) {
             const float y = x[i] * rstd;
             if (a.logits != nullptr) a.logits[static_cast<size_t>(r) * a.vocab + v] = y;
-            const uint32_t u = orderable(y);
+            const float score = T > 0.f ? y / T + row_gumbel(rkey, v) : y;
+            const uint32_t u = orderable(score);
             if (bidx == 0xffffffffu || u > best) {
                 best = u;
                 bidx = static_cast<uint32_t>(v);

@@ -757,8 +757,13 @@ int sdv_ensure_capacity(sdv_ctx *ctx, const int32_t *d_required, int B, void *st
                      d_required, B));
 }
 
-int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row_off, int B, int max_rows,
-                     int max_span, int32_t *d_argmax, float *d_logits, void *stream) {
+}  // extern "C"
+
+namespace {
+// The verify forward; temperature == nullptr: per-row argmax, else per-row draws (sampled verify).
+int spec_forward_impl(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row_off, int B, int max_rows,
+                      int max_span, int32_t *d_argmax, float *d_logits, const float *d_temperature,
+                      unsigned long long seed, void *stream) {
     if (!ctx || !d_tokens || !d_row_off || !d_argmax) return SDV_ERR_ARG;
     if (B <= 0 || B > ctx->c.max_batch || max_rows <= 0 || max_rows > ctx->c.max_rows || max_span <= 0 ||
         max_span > ctx->c.max_span || max_span > max_rows)
@@ -835,6 +840,10 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
     a.argmax_out = d_argmax;
     a.done_counter = ctx->done_lm;
     a.vocab = m.vocab;
+    a.temperature = d_temperature;
+    a.seed = seed;
+    a.row_seq = ctx->st.row_seq;
+    a.row_pos = ctx->st.row_pos;
     cudaError_t e;
     {
         PhaseMark pm(ctx, 6, st);
@@ -842,6 +851,23 @@ int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row
                         ctx->plan[P_LM].tiles * ctx->plan[P_LM].splits, st);
     }
     return e == cudaSuccess ? SDV_OK : SDV_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+int sdv_spec_forward(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row_off, int B, int max_rows,
+                     int max_span, int32_t *d_argmax, float *d_logits, void *stream) {
+    return spec_forward_impl(ctx, d_tokens, d_row_off, B, max_rows, max_span, d_argmax, d_logits, nullptr, 0,
+                             stream);
+}
+
+int sdv_spec_forward_sampled(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row_off, int B, int max_rows,
+                             int max_span, const float *d_temperature, uint64_t seed, int32_t *d_drawn,
+                             float *d_logits, void *stream) {
+    if (!d_temperature) return SDV_ERR_ARG;
+    return spec_forward_impl(ctx, d_tokens, d_row_off, B, max_rows, max_span, d_drawn, d_logits, d_temperature,
+                             seed, stream);
 }
 
 int sdv_accept_greedy(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_row_off, const int32_t *d_argmax,

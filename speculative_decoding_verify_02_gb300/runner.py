@@ -42,10 +42,12 @@ class SpecLoop:
         self.stream = torch.cuda.current_stream()
 
     # ------------------------------------------------------------------ prefill
-    def prefill(self, prompts, chunk: int = 128, ngram: bool = False):
+    def prefill(self, prompts, chunk: int = 128, ngram: bool = False, temperature=None, seed: int = 0):
         """Forward each prompt in chunks (sequence by sequence, a capacity
         reservation before each chunk); returns the first generated token of
-        each sequence (host numpy) and leaves it in self.first."""
+        each sequence (host numpy) and leaves it in self.first. With
+        `temperature` (a float32 device tensor [B]) the first token is drawn
+        by the sampled verify's sampler instead of taken as the argmax."""
         import torch
         B, v = self.B, self.v
         assert chunk <= v.ccfg.max_span and chunk <= v.ccfg.max_rows
@@ -69,7 +71,10 @@ class SpecLoop:
                 ro.copy_(torch.from_numpy(offs))
                 req.copy_(torch.from_numpy(r))
                 v.ensure_capacity(req, B)
-                v.spec_forward(tok, ro, B, max(n, 1), max(n, 1), am)
+                if temperature is None:
+                    v.spec_forward(tok, ro, B, max(n, 1), max(n, 1), am)
+                else:
+                    v.spec_forward_sampled(tok, ro, B, max(n, 1), max(n, 1), temperature, seed, am)
             first[b] = int(am[len(p) - 1 - (len(p) - 1) // chunk * chunk].item())
         self.first.copy_(torch.from_numpy(first))
         if ngram:
@@ -91,11 +96,18 @@ class SpecLoop:
         self.v.gen_init(self.first, self.budget, self.B, k_init, adaptive, k_max)
 
     # ------------------------------------------------------------------ one step
-    def step(self, drafter=SDV_DRAFT_NGRAM, table=None, table_stride=0, logits=None, ngram=True):
+    def step(self, drafter=SDV_DRAFT_NGRAM, table=None, table_stride=0, logits=None, ngram=True, temperature=None,
+             seed: int = 0):
+        """One transaction: propose, reserve, verify (greedy, or sampled at `temperature`, a float32
+        device tensor [B]), accept, rewind, and commit to the n-gram index."""
         v, B = self.v, self.B
         v.propose(drafter, table, table_stride, B, self.max_span, self.tokens, self.row_off, self.required)
         v.ensure_capacity(self.required, B)
-        v.spec_forward(self.tokens, self.row_off, B, self.max_rows, self.max_span, self.argmax, logits)
+        if temperature is None:
+            v.spec_forward(self.tokens, self.row_off, B, self.max_rows, self.max_span, self.argmax, logits)
+        else:
+            v.spec_forward_sampled(self.tokens, self.row_off, B, self.max_rows, self.max_span, temperature, seed,
+                                   self.argmax, logits)
         v.accept_greedy(self.tokens, self.row_off, self.argmax, B, self.max_span, self.n_accept, self.committed,
                         self.n_commit, self.new_len)
         v.rewind_cache(self.new_len, B)
