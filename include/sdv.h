@@ -68,10 +68,8 @@ typedef struct {
 } sdv_model_cfg;
 
 /* Cache and call limits. Attention takes its TMA-fed path when page_size is
- * a power of two in [8, 128], n_kv_heads <= 16 and max_context spans at most
- * 181 key groups of 1024 tokens at head_dim 128 (95 at 64: the merge across
- * 1024-position key groups is staged in shared memory); otherwise a slower
- * kernel that loads pages with ordinary loads serves the same calls. */
+ * a power of two in [8, 128] and n_kv_heads <= 16; otherwise a slower kernel
+ * that loads pages with ordinary loads serves the same calls. */
 typedef struct {
     int page_size;      /* tokens per KV page (16) */
     int n_pages;        /* pages in the pool */

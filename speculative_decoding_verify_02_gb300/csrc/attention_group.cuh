@@ -4,15 +4,16 @@
 //
 // A (sequence, 1024-position key group, kv head) is served by one thread-block cluster of
 // `splits` CTAs, each owning 8 / splits consecutive 128-key chunks of the group (the split is fixed
-// per context, so a row's arithmetic never depends on the span). A CTA walks its chunks in position
-// order with the next chunks' K/V copies in flight while the current chunk is computed, and keeps
-// an online softmax (running max m, sum l, unnormalised o) per query row. At most 32 query rows
-// (heads x span rows) per launch; warp w handles query tile w & 1 against the fixed 32-key quarter
-// w >> 1 of every chunk (all eight warps busy at verify widths). The quarter states stay in shared
-// memory; after a cluster barrier each CTA merges a slice of the rows over all splits x 4 states of
-// the group, reading the other CTAs' shared memory, in position order. With one key group that is
-// the output; with several, each group's state is parked in global memory and the last CTA of each
-// split index to arrive merges its rows over the groups, in group order.
+// per configuration, so a row's arithmetic never depends on the span or the batch). In each CTA one
+// producer warp issues the chunks' K/V copies into a ring of three buffers, refilling a buffer as
+// soon as every consumer warp released it, and eight consumer warps walk the chunks in position
+// order keeping an online softmax (running max m, sum l, unnormalised o) per query row. At most 32
+// query rows (heads x span rows) per launch; consumer warp w handles query tile w & 1 against the
+// fixed 32-key quarter w >> 1 of every chunk. The quarter states stay in shared memory; after a
+// cluster barrier each CTA merges a slice of the rows over all splits x 4 states of the group,
+// reading the other CTAs' shared memory, in position order. With one key group that is the output;
+// with several, each group's state is parked in global memory and attn_merge_kernel merges the
+// groups of every row, in group order, with one CTA per four rows.
 //
 // Keys are cut by position only and a chunk that is fully masked for a row leaves that row's
 // state exactly unchanged (scale 1, nothing added), so a row's result does not depend on how many
@@ -24,7 +25,8 @@
 
 namespace sdv {
 
-constexpr int kGrpThreads = 256;
+constexpr int kGrpConsumers = 256;                  // 8 warps: query tile x key quarter
+constexpr int kGrpThreads = kGrpConsumers + 32;      // + 1 producer warp that issues the K/V copies
 constexpr int kMaxKvHeads = 16;
 // the KV pool's tensor maps, one per kv head (kernel parameter space)
 struct KvMaps {
@@ -72,17 +74,15 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     extern __shared__ uint8_t sm_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sQ = sm;
-    __shared__ int page_s[kAttnGroup / 1 + 1];  // page of every position block of the group
-    __shared__ int last_s;
-    __shared__ __align__(8) uint64_t full[3];
+    __shared__ __align__(8) uint64_t full[S::NBUF], empty[S::NBUF];
 
     pdl_trigger();
     pdl_wait();
-    // optional timeline: 0 start, 1 Q and page ids in, 2 first chunk landed, 3 chunks done, 4 the
-    // CTA states of the cluster in place, 5 cluster merge done (output or parked group state),
-    // 8 merge across groups done (13 started, 14 and 15 thread 0's first element: maximum found,
-    // sums formed); 10 second chunk landed, 11 second chunk computed, 12 last chunk
-    // landed (when there are more than two)
+    // optional timeline: 0 start, 1 Q in, 2 first chunk landed, 3 chunks done, 4 the CTA states of
+    // the cluster in place, 5 cluster merge done (output or parked group state), 6 CTA end; 10 second
+    // chunk landed, 11 second chunk computed, 12 last chunk landed (when there are more than two);
+    // the CTA merging across key groups: 13 merge started, 14 group weights staged, 15 first
+    // element summed, 8 merge done
     auto stamp = [&](int ev) {
         if (a.trace && threadIdx.x == 0)
             a.trace[((static_cast<size_t>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * 16 + ev] =
@@ -108,72 +108,66 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     const int c_lo = sp * c_per, c_hi = min(c_lo + c_per, n_ch_group);  // this CTA's chunks (may be none)
     const int n_ch = max(0, c_hi - c_lo);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool consumer = tid < kGrpConsumers;
     const bool has_lo = a.q_plane != 0;
     const int lp = 31 - __clz(a.page_size);  // page size: a power of two in [8, 128]
 
-    // Q rows j = i_local * grp + hh (span row q0 + i_local, head g*grp + hh), both planes
-    for (int e = tid; e < 2 * Mpad * CH; e += kGrpThreads) {
-        const int pl = e / (Mpad * CH), j = (e / CH) % Mpad, c = e % CH;
-        const bool valid = j < M && (pl == 0 || has_lo);
-        const bf16 *src = a.q;
-        if (valid) {
-            const int r = row0 + a.q0 + j / a.grp;
-            const int h = g * a.grp + j % a.grp;
-            src = a.q + pl * a.q_plane + (static_cast<size_t>(r) * a.nq + h) * D + c * 8;
-        }
-        cp_async16(smem_u32(sQ) + swz<D>(pl * kGrpRows + j, c), src, valid);
-    }
-    cp_async_commit();
     if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
-        mbar_init(&full[2], 1);
+        for (int i = 0; i < S::NBUF; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kGrpConsumers / 32);  // one arrival per consumer warp
+        }
         fence_mbar_init();
-        prefetch_tensormap(&tkv.m[g]);
-    }
-    const int pg0 = g0 / a.page_size, npg = (g1 - 1) / a.page_size - pg0 + 1;
-    for (int i = tid; i < npg; i += kGrpThreads) {
-        const int slot_idx = pg0 + i;
-        page_s[i] = slot_idx < a.pages_per_seq ? a.page_table[static_cast<size_t>(b) * a.pages_per_seq + slot_idx] : -1;
     }
     __syncthreads();
 
-    // one chunk's K and V: per page of the chunk one box (K and V rows of head g, both 64-dim
-    // halves); the lanes of warp 0 issue them after lane 0 has posted the byte count
-    const int ppc = kAttnChunk / a.page_size;  // pages per chunk
-    auto load_chunk = [&](int ch, int buf) {  // ch: this CTA's chunk index
-        if (warp != 0) return;
-        uint8_t *kb = sm + S::BUF_OFF + buf * 2 * S::KV_BYTES;
-        const int k0 = g0 + (c_lo + ch) * kAttnChunk, k1 = min(k0 + kAttnChunk, g1);
-        const int p_first = k0 / a.page_size - pg0, p_last = (k1 - 1) / a.page_size - pg0;
-        const int box_bytes = 2 * a.page_size * D * 2;  // one head's K and V rows of a page
-        int bytes = 0;
-        for (int pi = p_first + lane; pi <= p_last; pi += 32) {
-            const int page = page_s[pi];
-            if (page >= 0 && page < a.n_pages) bytes += box_bytes;
-        }
-        bytes = __reduce_add_sync(0xffffffffu, bytes);
+    if (!consumer) {
+        // Producer warp: one chunk's K and V is one box per page of the chunk (K and V rows of head
+        // g, both 64-dim halves, 8 KB at page size 16), issued by the lanes after lane 0 has
+        // posted the byte count; a buffer is refilled once every consumer warp released it. The
+        // page ids come straight from the page table, so the first copies start while Q loads.
+        prefetch_tensormap(&tkv.m[g]);
         const uint64_t pol_kv = policy_evict_first();  // K/V are read once per step: keep L2 for the rest
-        if (lane == 0) mbar_arrive_expect_tx(&full[buf], static_cast<uint32_t>(bytes));
-        __syncwarp();
-        for (int pi = p_first + lane; pi <= p_last; pi += 32) {
-            const int page = page_s[pi];
-            if (page < 0 || page >= a.n_pages) {
-                set_status(a.status, SDV_ERR_CAPACITY);
-                continue;
+        const int box_bytes = 2 * a.page_size * D * 2;
+        for (int ch = 0; ch < n_ch; ++ch) {
+            const int buf = ch % S::NBUF;
+            if (ch >= S::NBUF && !mbar_wait(&empty[buf], ((ch / S::NBUF) - 1) & 1)) {
+                if (lane == 0) set_status(a.status, SDV_ERR_DEVICE_TIMEOUT);
+                break;
             }
-            tma_load_5d_hint(kb + (pi - p_first) * box_bytes, &tkv.m[g], &full[buf], 0, 0, 0, 0,
-                             a.layer * a.n_pages + page, pol_kv);
+            uint8_t *kb = sm + S::BUF_OFF + buf * 2 * S::KV_BYTES;
+            const int k0 = g0 + (c_lo + ch) * kAttnChunk, k1 = min(k0 + kAttnChunk, g1);
+            const int s_first = k0 / a.page_size, s_last = (k1 - 1) / a.page_size;  // page-table slots
+            int page = -1;
+            const int si = s_first + lane;
+            if (si <= s_last && si < a.pages_per_seq) page = a.page_table[static_cast<size_t>(b) * a.pages_per_seq + si];
+            const bool ok = page >= 0 && page < a.n_pages;
+            if (si <= s_last && !ok) set_status(a.status, SDV_ERR_CAPACITY);
+            const int bytes = __reduce_add_sync(0xffffffffu, ok ? box_bytes : 0);
+            if (lane == 0) mbar_arrive_expect_tx(&full[buf], static_cast<uint32_t>(bytes));
+            __syncwarp();
+            if (ok)
+                tma_load_5d_hint(kb + (si - s_first) * box_bytes, &tkv.m[g], &full[buf], 0, 0, 0, 0,
+                                 a.layer * a.n_pages + page, pol_kv);
         }
-    };
-    __syncthreads();  // barriers initialised, page ids in place
-    if (n_ch > 0) load_chunk(0, 0);
-    if (n_ch > 1) load_chunk(1, 1);
-    if (n_ch > 2) load_chunk(2, 2);
-    cp_async_wait_all();  // Q
-    __syncthreads();
-    stamp(1);
-    (void)ppc;
+    } else {
+        // Q rows j = i_local * grp + hh (span row q0 + i_local, head g*grp + hh), both planes
+        for (int e = tid; e < 2 * Mpad * CH; e += kGrpConsumers) {
+            const int pl = e / (Mpad * CH), j = (e / CH) % Mpad, c = e % CH;
+            const bool valid = j < M && (pl == 0 || has_lo);
+            const bf16 *src = a.q;
+            if (valid) {
+                const int r = row0 + a.q0 + j / a.grp;
+                const int h = g * a.grp + j % a.grp;
+                src = a.q + pl * a.q_plane + (static_cast<size_t>(r) * a.nq + h) * D + c * 8;
+            }
+            cp_async16(smem_u32(sQ) + swz<D>(pl * kGrpRows + j, c), src, valid);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        named_bar_sync(1, kGrpConsumers);  // Q in place for every consumer warp
+        stamp(1);
+    }
 
     // warp w: query tile mt = w & 1 (16 of the <= 32 rows), 32-key quarter kq = w >> 1 of every chunk
     const int mt = warp & 1, kq = warp >> 1;
@@ -186,7 +180,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-    for (int ch = 0; ch < n_ch; ++ch) {
+    for (int ch = 0; consumer && ch < n_ch; ++ch) {
         const int buf = ch % S::NBUF;
         if (!mbar_wait(&full[buf], (ch / S::NBUF) & 1)) set_status(a.status, SDV_ERR_DEVICE_TIMEOUT);
         if (ch == 0) stamp(2);
@@ -195,17 +189,20 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         const uint32_t sKV = smem_u32(sm + S::BUF_OFF + buf * 2 * S::KV_BYTES);
         {   // keys past the group end read as zero V rows (the pool holds stale data there)
             const int kstart = g0 + (c_lo + ch) * kAttnChunk, nvalid = min(kAttnChunk, g1 - kstart);
-            for (int e = tid; e < (kAttnChunk - nvalid) * CH; e += kGrpThreads) {
-                const int r = nvalid + e / CH, c = e % CH;
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sKV + swz_kv<D>(r, c, 1, lp)), "r"(0u) : "memory");
+            if (nvalid < kAttnChunk) {  // the same for every consumer warp
+                for (int e = tid; e < (kAttnChunk - nvalid) * CH; e += kGrpConsumers) {
+                    const int r = nvalid + e / CH, c = e % CH;
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sKV + swz_kv<D>(r, c, 1, lp)), "r"(0u) : "memory");
+                }
+                named_bar_sync(1, kGrpConsumers);
             }
         }
-        __syncthreads();
         const int ubase = g0 + (c_lo + ch) * kAttnChunk + kq * kGrpQKeys;
         if (active && ubase < g1) {
-            float s[4][4];
+            float s[4][4], t[4][4];  // q_hi . k and q_lo . k, summed after the k loop
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+            for (int nt = 0; nt < 4; ++nt)
+                s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = t[nt][0] = t[nt][1] = t[nt][2] = t[nt][3] = 0.f;
 #pragma unroll 2
             for (int ks = 0; ks < D / 16; ++ks) {
                 uint32_t qh[4], ql[4];
@@ -225,10 +222,17 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
                     mma_bf16_16816(s[nt], qh, b0, b1);
                     mma_bf16_16816(s[nt + 1], qh, b2, b3);
                     if (has_lo) {
-                        mma_bf16_16816(s[nt], ql, b0, b1);
-                        mma_bf16_16816(s[nt + 1], ql, b2, b3);
+                        mma_bf16_16816(t[nt], ql, b0, b1);
+                        mma_bf16_16816(t[nt + 1], ql, b2, b3);
                     }
                 }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                s[nt][0] += t[nt][0];
+                s[nt][1] += t[nt][1];
+                s[nt][2] += t[nt][2];
+                s[nt][3] += t[nt][3];
             }
             // mask (position < group end and <= the row's causal limit), running max (log2 domain)
             float mx0 = m0, mx1 = m1;
@@ -301,15 +305,17 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         }
         if (ch == 1) stamp(11);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic accesses before the refill
-        __syncthreads();  // buffer `buf` is free
-        if (ch + S::NBUF < n_ch) load_chunk(ch + S::NBUF, buf);
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[buf])) : "memory");
     }
+    // every chunk consumed by every consumer warp (no copy in flight) before the buffers are reused
+    __syncthreads();
 
     stamp(3);
     // the four quarters' states -> shared memory: per [quarter][row] a row of QO_LD floats holding
     // the unnormalised o, then (m, l) at D, D + 1; quarters without keys keep (-inf, 0, 0)
     float *qo = reinterpret_cast<float *>(sm + S::BUF_OFF);
-    if (mt * 16 < Mpad) {
+    if (consumer && mt * 16 < Mpad) {
         float *dst = qo + static_cast<size_t>(kq) * kGrpRows * S::QO_LD;
 #pragma unroll
         for (int dn = 0; dn < D / 8; ++dn) {
@@ -412,92 +418,70 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     }
     cluster_arrive();  // this CTA's reads of the other CTAs' shared memory are done
     stamp(5);
-    if (multi) {
-        // the last of the key groups' CTAs with this split index merges rows [j0, j1) over the
-        // groups' parked states, in group order
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            int *cnt = &a.counters[(b * a.nkv + g) * kAttnCluster + sp];
-            const int last = atomicAdd(cnt, 1) == n_groups - 1;
-            if (last) *cnt = 0;
-            last_s = last;
-        }
-        __syncthreads();
-        if (last_s) {
-            __threadfence();
-            stamp(13);
-            const int wfirst = w - grp_idx;  // the work items of one sequence are consecutive
-            const int nr = j1 - j0;
-            auto slot_of = [&](int q) { return (static_cast<size_t>(wfirst) + q) * a.nkv + g; };
-            // the groups' (m, l) of the slice's rows -> shared memory (the quarter-state region, no
-            // longer read); per row the maximum, each group's weight and the denominator (a warp per
-            // row, lanes over groups, group order kept by the fixed shuffle tree); then each thread
-            // sums float4 columns over the groups with a batch of loads in flight
-            if (n_groups * nr * 12 + nr * 4 > S::RECV_OFF) {  // the host keeps contexts within this
-                if (tid == 0) set_status(a.status, SDV_ERR_UNSUPPORTED);
-            } else {
-            float2 *gml = reinterpret_cast<float2 *>(qo);                 // [group][nr]
-            float *gw = reinterpret_cast<float *>(gml + n_groups * nr);   // [group][nr]
-            float *gden = gw + n_groups * nr;                             // [nr]
-            for (int e = tid; e < n_groups * nr; e += kGrpThreads) {
-                const int q = e / nr, r = e - q * nr;
-                gml[e] = __ldcg(&a.part_ml[slot_of(q) * rowsw + j0 + r]);
-            }
-            __syncthreads();
-            for (int r = warp; r < nr; r += kGrpThreads / 32) {
-                float Mx = -INFINITY;
-                for (int q = lane; q < n_groups; q += 32) Mx = fmaxf(Mx, gml[q * nr + r].x);
-#pragma unroll
-                for (int o2 = 16; o2 > 0; o2 >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o2));
-                float den = 0.f;
-                for (int q = lane; q < n_groups; q += 32) {
-                    const float2 st = gml[q * nr + r];
-                    const float wq = st.x == -INFINITY ? 0.f : exp2f(st.x - Mx);
-                    gw[q * nr + r] = wq;
-                    den += wq * st.y;
-                }
-#pragma unroll
-                for (int o2 = 16; o2 > 0; o2 >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o2);
-                if (lane == 0) gden[r] = den;
-            }
-            __syncthreads();
-            stamp(14);
-            for (int it = tid; it < nr * (D / 4); it += kGrpThreads) {
-                const int r = it / (D / 4), j = j0 + r, d = (it % (D / 4)) * 4;
-                constexpr int QB = 16;  // groups whose loads are in flight together
-                float4 n = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int q0 = 0; q0 < n_groups; q0 += QB) {
-                    float4 x[QB];
-#pragma unroll
-                    for (int k = 0; k < QB; ++k)
-                        x[k] = q0 + k < n_groups
-                                   ? __ldcg(reinterpret_cast<const float4 *>(&a.part_o[(slot_of(q0 + k) * rowsw + j) * D + d]))
-                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int k = 0; k < QB; ++k) {
-                        if (q0 + k < n_groups) {  // group order
-                            const float wq = gw[(q0 + k) * nr + r];
-                            n.x += wq * x[k].x;
-                            n.y += wq * x[k].y;
-                            n.z += wq * x[k].z;
-                            n.w += wq * x[k].w;
-                        }
-                    }
-                }
-                if (it == 0) stamp(15);
-                const float den = gden[r];
-                store(j, d, n.x / den);
-                store(j, d + 1, n.y / den);
-                store(j, d + 2, n.z / den);
-                store(j, d + 3, n.w / den);
-            }
-            }
-            stamp(8);
-        }
-    }
     cluster_wait();  // no CTA leaves while another may still read its shared memory
     stamp(6);
+}
+
+// Merge across key groups (sequences longer than one 1024-position group): each group's state
+// (unnormalised o, running max m, sum l) was parked by its cluster; CTA (slice, kv head g,
+// sequence b) finishes kMergeRows query rows: per row the maximum over the groups, each group's
+// weight 2^(m_q - max) (0 for a group with no key at or before the row), and the weighted sums of
+// l and o in group order. A sequence of one group was written by the attention kernel itself.
+constexpr int kMergeRows = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeRows * D / 4)
+    attn_merge_kernel(const AttnArgs a, const int *work_off) {
+    pdl_trigger();
+    pdl_wait();
+    const int b = blockIdx.z, g = blockIdx.y;
+    const int w0 = work_off[b], n_groups = work_off[b + 1] - w0;
+    if (n_groups <= 1) return;
+    const int4 wi = a.work[w0];
+    const int S_b = wi.z, row0 = wi.w;
+    const int ni = max(0, min(S_b - a.q0, a.qrows));
+    const int M = a.grp * ni;
+    const int j = blockIdx.x * kMergeRows + static_cast<int>(threadIdx.x) / (D / 4);
+    const int d = (static_cast<int>(threadIdx.x) % (D / 4)) * 4;
+    if (j >= M) return;
+    const size_t rowsw = static_cast<size_t>(a.grp) * a.qrows;
+    auto slot = [&](int q) { return ((static_cast<size_t>(w0) + q) * a.nkv + g) * rowsw + j; };
+    float Mx = -INFINITY;
+    for (int q = 0; q < n_groups; ++q) Mx = fmaxf(Mx, __ldcg(&a.part_ml[slot(q)]).x);
+    float den = 0.f;
+    float4 n = make_float4(0.f, 0.f, 0.f, 0.f);
+    constexpr int QB = 8;  // groups whose loads are in flight together
+    for (int q0 = 0; q0 < n_groups; q0 += QB) {
+        float2 ml[QB];
+        float4 x[QB];
+#pragma unroll
+        for (int k = 0; k < QB; ++k) {
+            if (q0 + k < n_groups) {
+                ml[k] = __ldcg(&a.part_ml[slot(q0 + k)]);
+                x[k] = __ldcg(reinterpret_cast<const float4 *>(&a.part_o[slot(q0 + k) * D + d]));
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < QB; ++k) {
+            if (q0 + k < n_groups) {  // group order
+                const float wq = ml[k].x == -INFINITY ? 0.f : exp2f(ml[k].x - Mx);
+                den += wq * ml[k].y;
+                n.x += wq * x[k].x;
+                n.y += wq * x[k].y;
+                n.z += wq * x[k].z;
+                n.w += wq * x[k].w;
+            }
+        }
+    }
+    const int r = row0 + a.q0 + j / a.grp, h = g * a.grp + j % a.grp;
+    const size_t oi = (static_cast<size_t>(r) * a.nq + h) * D + d;
+    const float v[4] = {n.x / den, n.y / den, n.z / den, n.w / den};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const Bf16Pair pr = split_bf16(v[i]);
+        a.out[oi + i] = pr.hi;
+        if (a.out_plane) a.out[oi + i + a.out_plane] = pr.lo;
+    }
 }
 
 }  // namespace sdv

@@ -488,8 +488,8 @@ GemmArgs base_args(const sdv_ctx *ctx, int kind, int pidx, int layer) {
 }
 
 // Paged attention of `layer` over the rows prepared in the device state.
-int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *out, size_t out_plane, int max_span,
-                  cudaStream_t st) {
+int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *out, size_t out_plane, int B,
+                  int max_span, cudaStream_t st) {
     const sdv_model_cfg &m = ctx->m;
     AttnArgs a{};
     a.q = q;
@@ -539,6 +539,9 @@ int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *
     // at most kGrpRows query rows per launch (attention_group.cuh)
     const dim3 grid(ctx->attn_splits, m.n_kv_heads, ctx->work_cap);
     a.qrows = std::max(1, kGrpRows / ctx->grp);
+    // sequences longer than one key group: their groups' states are merged by attn_merge_kernel
+    const bool merge = ceil_div(static_cast<long long>(ctx->c.max_context), kAttnGroup) > 1;
+    const dim3 mgrid(ceil_div(kGrpRows, kMergeRows), m.n_kv_heads, B);
     for (int q0 = 0; q0 < max_span; q0 += a.qrows) {
         a.q0 = q0;
         cudaError_t e;
@@ -548,6 +551,13 @@ int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *
         else
             e = launch_cluster(ctx, attn_group_kernel<64>, grid, dim3(kGrpThreads), GrpShape<64>::SMEM, st,
                                ctx->attn_splits, a, ctx->tm_kv);
+        if (e == cudaSuccess && merge) {
+            const int *work_off = ctx->st.work_off;
+            if (m.head_dim == 128)
+                e = launch(ctx, attn_merge_kernel<128>, mgrid, dim3(kMergeRows * 128 / 4), 0, st, a, work_off);
+            else
+                e = launch(ctx, attn_merge_kernel<64>, mgrid, dim3(kMergeRows * 64 / 4), 0, st, a, work_off);
+        }
         if (e != cudaSuccess) return SDV_ERR_CUDA;
     }
     return SDV_OK;
@@ -688,12 +698,8 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
         ok &= encode_2d(&ctx->tm_wd[l], L.w_down, H, F, 128);
     }
     ok &= encode_2d(&ctx->tm_lm, w->lm_head, m->vocab, H, 128);
-    // the group kernel stages the merge across key groups in its quarter-state region
-    const int grp_stage = m->head_dim == 128 ? GrpShape<128>::RECV_OFF : GrpShape<64>::RECV_OFF;
     ctx->attn_tma = c->page_size >= 8 && c->page_size <= kAttnChunk && (c->page_size & (c->page_size - 1)) == 0 &&
-                    m->n_kv_heads <= kMaxKvHeads &&
-                    static_cast<long long>(ceil_div(c->max_context, kAttnGroup)) * kGrpRows * 12 + kGrpRows * 4 <=
-                        grp_stage;
+                    m->n_kv_heads <= kMaxKvHeads;
     if (ctx->attn_tma) ok &= encode_pool(&ctx->tm_kv, d_kv_pool, *m, *c);
     for (int i = 0; i < 4 && ok; ++i) {
         ok &= encode_planes(&ctx->tm_xb[i], ctx->xb, kRowsCap, H, kNs[i]);
@@ -791,7 +797,7 @@ int spec_forward_impl(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_ro
         {
             PhaseMark pm(ctx, 2, st);
             const size_t plane = static_cast<size_t>(kRowsCap) * m.n_q_heads * m.head_dim;
-            r = run_attention(ctx, l, ctx->q, plane, ctx->attn_o, plane, max_span, st);
+            r = run_attention(ctx, l, ctx->q, plane, ctx->attn_o, plane, B, max_span, st);
         }
         if (r) return r;
         // O projection + residual; emits bf16(x * g_ffn) and sum-of-squares parts. Its weights
@@ -1024,7 +1030,7 @@ int sdv_op_attention(sdv_ctx *ctx, int layer, const void *d_q, const int32_t *d_
     const int max_rows = ctx->c.max_rows;
     int r = prepare(ctx, nullptr, d_row_off, d_base, B, max_rows, max_span, 0, st);
     if (r) return r;
-    return run_attention(ctx, layer, static_cast<const bf16 *>(d_q), 0, static_cast<bf16 *>(d_out), 0, max_span, st);
+    return run_attention(ctx, layer, static_cast<const bf16 *>(d_q), 0, static_cast<bf16 *>(d_out), 0, B, max_span, st);
 }
 
 }  // extern "C"
