@@ -12,8 +12,9 @@
 // fixed 32-key quarter w >> 1 of every chunk. The quarter states stay in shared memory; after a
 // cluster barrier each CTA merges a slice of the rows over all splits x 4 states of the group,
 // reading the other CTAs' shared memory, in position order. With one key group that is the output;
-// with several, each group's state is parked in global memory and attn_merge_kernel merges the
-// groups of every row, in group order, with one CTA per four rows.
+// with several, each group's state is parked in global memory and merged across the groups, in
+// group order: up to 8 groups by the last group CTA of each split index to finish, longer
+// sequences by attn_merge_kernel with one CTA per four rows.
 //
 // Keys are cut by position only and a chunk that is fully masked for a row leaves that row's
 // state exactly unchanged (scale 1, nothing added), so a row's result does not depend on how many
@@ -36,6 +37,9 @@ constexpr int kGrpChunks = kAttnGroup / kAttnChunk;  // 8 chunks of 128 keys
 constexpr int kGrpRows = 32;                         // query rows (heads x span rows) per launch
 constexpr int kGrpQuarters = 4;                      // fixed key partition of a chunk
 constexpr int kGrpQKeys = kAttnChunk / kGrpQuarters;
+// sequences of up to this many 1024-position key groups are merged across groups inside the
+// attention kernel (by the last group CTA to finish); longer ones by attn_merge_kernel
+constexpr int kInKernelMergeGroups = 8;
 
 template <int D>
 struct GrpShape {
@@ -75,6 +79,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sQ = sm;
     __shared__ __align__(8) uint64_t full[S::NBUF], empty[S::NBUF];
+    __shared__ int last_s;
 
     pdl_trigger();
     pdl_wait();
@@ -418,15 +423,98 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     }
     cluster_arrive();  // this CTA's reads of the other CTAs' shared memory are done
     stamp(5);
+    if (multi && n_groups <= kInKernelMergeGroups) {
+        // up to kInKernelMergeGroups groups: the last of the groups' CTAs with this split index
+        // merges rows [j0, j1) over the groups' parked states, in group order (longer sequences are
+        // merged by attn_merge_kernel)
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            int *cnt = &a.counters[(b * a.nkv + g) * kAttnCluster + sp];
+            const int last = atomicAdd(cnt, 1) == n_groups - 1;
+            if (last) *cnt = 0;
+            last_s = last;
+        }
+        __syncthreads();
+        if (last_s) {
+            __threadfence();
+            stamp(13);
+            const int wfirst = w - grp_idx;  // the work items of one sequence are consecutive
+            const int nr = j1 - j0;
+            auto slot_of = [&](int q) { return (static_cast<size_t>(wfirst) + q) * a.nkv + g; };
+            // per row: the maximum over the groups, each group's weight and the denominator, staged
+            // in shared memory (the quarter-state region, no longer read)
+            float *gw = qo;                                            // [group][nr]
+            float *gden = gw + kInKernelMergeGroups * kGrpRows;        // [nr]
+            for (int r = tid; r < nr; r += kGrpThreads) {
+                float2 st[kInKernelMergeGroups];
+                float Mx = -INFINITY;
+#pragma unroll
+                for (int q = 0; q < kInKernelMergeGroups; ++q)
+                    if (q < n_groups) {
+                        st[q] = __ldcg(&a.part_ml[slot_of(q) * rowsw + j0 + r]);
+                        Mx = fmaxf(Mx, st[q].x);
+                    }
+                float den = 0.f;
+#pragma unroll
+                for (int q = 0; q < kInKernelMergeGroups; ++q)
+                    if (q < n_groups) {
+                        const float wq = st[q].x == -INFINITY ? 0.f : exp2f(st[q].x - Mx);
+                        gw[q * nr + r] = wq;
+                        den += wq * st[q].y;
+                    }
+                gden[r] = den;
+            }
+            __syncthreads();
+            stamp(14);
+            // two float4 columns per thread and pass, every group's load in flight together
+            for (int it0 = tid; it0 < nr * (D / 4); it0 += 2 * kGrpThreads) {
+                float4 x[2][kInKernelMergeGroups];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int it = it0 + u * kGrpThreads;
+                    const int j = j0 + it / (D / 4), d = (it % (D / 4)) * 4;
+#pragma unroll
+                    for (int q = 0; q < kInKernelMergeGroups; ++q)
+                        if (it < nr * (D / 4) && q < n_groups)
+                            x[u][q] = __ldcg(reinterpret_cast<const float4 *>(&a.part_o[(slot_of(q) * rowsw + j) * D + d]));
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int it = it0 + u * kGrpThreads;
+                    if (it >= nr * (D / 4)) break;
+                    const int r = it / (D / 4), j = j0 + r, d = (it % (D / 4)) * 4;
+                    float4 n = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int q = 0; q < kInKernelMergeGroups; ++q) {
+                        if (q < n_groups) {  // group order
+                            const float wq = gw[q * nr + r];
+                            n.x += wq * x[u][q].x;
+                            n.y += wq * x[u][q].y;
+                            n.z += wq * x[u][q].z;
+                            n.w += wq * x[u][q].w;
+                        }
+                    }
+                    if (it == 0) stamp(15);
+                    const float den = gden[r];
+                    store(j, d, n.x / den);
+                    store(j, d + 1, n.y / den);
+                    store(j, d + 2, n.z / den);
+                    store(j, d + 3, n.w / den);
+                }
+            }
+            stamp(8);
+        }
+    }
     cluster_wait();  // no CTA leaves while another may still read its shared memory
     stamp(6);
 }
 
-// Merge across key groups (sequences longer than one 1024-position group): each group's state
+// Merge across key groups (sequences of more than kInKernelMergeGroups groups): each group's state
 // (unnormalised o, running max m, sum l) was parked by its cluster; CTA (slice, kv head g,
 // sequence b) finishes kMergeRows query rows: per row the maximum over the groups, each group's
 // weight 2^(m_q - max) (0 for a group with no key at or before the row), and the weighted sums of
-// l and o in group order. A sequence of one group was written by the attention kernel itself.
+// l and o in group order. Shorter sequences were finished by the attention kernel itself.
 constexpr int kMergeRows = 4;
 
 template <int D>
@@ -436,7 +524,7 @@ __global__ void __launch_bounds__(kMergeRows * D / 4)
     pdl_wait();
     const int b = blockIdx.z, g = blockIdx.y;
     const int w0 = work_off[b], n_groups = work_off[b + 1] - w0;
-    if (n_groups <= 1) return;
+    if (n_groups <= kInKernelMergeGroups) return;  // merged inside the attention kernel
     const int4 wi = a.work[w0];
     const int S_b = wi.z, row0 = wi.w;
     const int ni = max(0, min(S_b - a.q0, a.qrows));

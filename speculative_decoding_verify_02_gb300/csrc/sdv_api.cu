@@ -539,8 +539,8 @@ int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *
     // at most kGrpRows query rows per launch (attention_group.cuh)
     const dim3 grid(ctx->attn_splits, m.n_kv_heads, ctx->work_cap);
     a.qrows = std::max(1, kGrpRows / ctx->grp);
-    // sequences longer than one key group: their groups' states are merged by attn_merge_kernel
-    const bool merge = ceil_div(static_cast<long long>(ctx->c.max_context), kAttnGroup) > 1;
+    // sequences of more key groups than the attention kernel merges itself: attn_merge_kernel
+    const bool merge = ceil_div(static_cast<long long>(ctx->c.max_context), kAttnGroup) > kInKernelMergeGroups;
     const dim3 mgrid(ceil_div(kGrpRows, kMergeRows), m.n_kv_heads, B);
     for (int q0 = 0; q0 < max_span; q0 += a.qrows) {
         a.q0 = q0;

@@ -49,18 +49,31 @@ def test_attention_batch16_multigroup_against_oracle(spans):
     bf16 K/V and queries: every output row of every sequence against the oracle's attention on
     the same values. The ragged case mixes spans of 1..17 rows (up to three launches of 8 span
     rows at 4 q heads per kv head)."""
+    lens = [int(n) for n in workloads.context_lengths(3, 16)]
+    S = [8] * 16 if spans == "uniform8" else [1, 17, 8, 3, 12, 5, 9, 2, 16, 7, 4, 11, 6, 10, 13, 1]
+    assert max(lens) > 3 * 1024
+    _attention_batch(lens, S, max(lens) + 32, spans)
+
+
+def test_attention_mixed_merge_paths():
+    """One launch holding sequences of 1, 3, 9 and 20 key groups under a 24K-token configuration:
+    up to 8 groups are merged inside the attention kernel, longer sequences by the separate merge
+    kernel; every row against the oracle."""
+    _attention_batch([700, 2500, 9000, 20000], [8, 3, 17, 8], 24576, "mixed")
+
+
+def _attention_batch(lens, S, max_context, tag):
     import torch
     import speculative_decoding_verify_02_gb300 as sdv
     shape = synth.Shape("attn-4b-heads", 1, 256, 32, 8, 128, 256, 256)     # the 4B model's heads
     weights = {n: torch.zeros(d, dtype=torch.bfloat16, device="cuda") for n, d in shape.tensor_shapes().items()}
-    B = 16
-    lens = [int(n) for n in workloads.context_lengths(3, B)]
-    S = [8] * B if spans == "uniform8" else [1, 17, 8, 3, 12, 5, 9, 2, 16, 7, 4, 11, 6, 10, 13, 1]
+    B = len(lens)
+    spans = tag
     R = sum(S)
-    assert R <= 128 and max(lens) > 3 * 1024
+    assert R <= 128
     need = sum(-(-(L + s) // P) for L, s in zip(lens, S))
     v = sdv.Verifier(shape, weights, page_size=P, n_pages=need + 8, max_batch=B, max_rows=128, max_span=17,
-                     max_context=max(lens) + 32)
+                     max_context=max_context)
     v.ensure_capacity(_t([L + s for L, s in zip(lens, S)]), B)
     tab, _, _ = page_tables(v)
     nkv, nq, D = 8, 32, 128
