@@ -42,6 +42,8 @@ struct AttnArgs {
     int splits;              // attention_group.cuh: CTAs sharing one group's chunks (1, 2, 4 or 8)
     int p_lo;                // attention_group.cuh: 1 = probabilities as a hi/lo pair, 0 = bf16 only
     int layer;               // attention_group.cuh: layer index in the pool tensor map
+    int merge_groups;        // attention_group.cuh: sequences of up to this many key groups are merged
+                             // inside the attention kernel; longer ones by attn_merge_kernel
     unsigned long long *trace;  // attention_group.cuh: optional [CTA][8] %globaltimer stamps, or nullptr
 };
 

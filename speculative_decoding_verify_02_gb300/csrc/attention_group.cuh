@@ -13,8 +13,9 @@
 // cluster barrier each CTA merges a slice of the rows over all splits x 4 states of the group,
 // reading the other CTAs' shared memory, in position order. With one key group that is the output;
 // with several, each group's state is parked in global memory and merged across the groups, in
-// group order: up to 8 groups by the last group CTA of each split index to finish, longer
-// sequences by attn_merge_kernel with one CTA per four rows.
+// group order: when a group's cluster has at least four CTAs, sequences of up to 8 groups by the
+// last group CTA of each split index to finish (a few rows each); every other multi-group
+// sequence by attn_merge_kernel, with one CTA per four rows.
 //
 // Keys are cut by position only and a chunk that is fully masked for a row leaves that row's
 // state exactly unchanged (scale 1, nothing added), so a row's result does not depend on how many
@@ -423,10 +424,10 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     }
     cluster_arrive();  // this CTA's reads of the other CTAs' shared memory are done
     stamp(5);
-    if (multi && n_groups <= kInKernelMergeGroups) {
-        // up to kInKernelMergeGroups groups: the last of the groups' CTAs with this split index
-        // merges rows [j0, j1) over the groups' parked states, in group order (longer sequences are
-        // merged by attn_merge_kernel)
+    if (multi && n_groups <= a.merge_groups) {
+        // up to a.merge_groups (<= kInKernelMergeGroups) groups: the last of the groups' CTAs with
+        // this split index merges rows [j0, j1) over the groups' parked states, in group order
+        // (other sequences are merged by attn_merge_kernel)
         __threadfence();
         __syncthreads();
         if (tid == 0) {
@@ -524,7 +525,7 @@ __global__ void __launch_bounds__(kMergeRows * D / 4)
     pdl_wait();
     const int b = blockIdx.z, g = blockIdx.y;
     const int w0 = work_off[b], n_groups = work_off[b + 1] - w0;
-    if (n_groups <= kInKernelMergeGroups) return;  // merged inside the attention kernel
+    if (n_groups <= 1 || n_groups <= a.merge_groups) return;  // one group, or merged in the attention kernel
     const int4 wi = a.work[w0];
     const int S_b = wi.z, row0 = wi.w;
     const int ni = max(0, min(S_b - a.q0, a.qrows));

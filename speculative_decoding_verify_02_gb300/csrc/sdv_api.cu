@@ -539,8 +539,11 @@ int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *
     // at most kGrpRows query rows per launch (attention_group.cuh)
     const dim3 grid(ctx->attn_splits, m.n_kv_heads, ctx->work_cap);
     a.qrows = std::max(1, kGrpRows / ctx->grp);
-    // sequences of more key groups than the attention kernel merges itself: attn_merge_kernel
-    const bool merge = ceil_div(static_cast<long long>(ctx->c.max_context), kAttnGroup) > kInKernelMergeGroups;
+    // Merge across key groups: inside the attention kernel when a group's cluster has at least four
+    // CTAs to share the rows (up to kInKernelMergeGroups groups), else by attn_merge_kernel, which
+    // is launched only when the configuration allows such sequences.
+    a.merge_groups = ctx->attn_splits >= 4 ? kInKernelMergeGroups : 1;
+    const bool merge = ceil_div(static_cast<long long>(ctx->c.max_context), kAttnGroup) > a.merge_groups;
     const dim3 mgrid(ceil_div(kGrpRows, kMergeRows), m.n_kv_heads, B);
     for (int q0 = 0; q0 < max_span; q0 += a.qrows) {
         a.q0 = q0;

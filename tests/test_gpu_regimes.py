@@ -55,11 +55,17 @@ def test_attention_batch16_multigroup_against_oracle(spans):
     _attention_batch(lens, S, max(lens) + 32, spans)
 
 
-def test_attention_mixed_merge_paths():
-    """One launch holding sequences of 1, 3, 9 and 20 key groups under a 24K-token configuration:
-    up to 8 groups are merged inside the attention kernel, longer sequences by the separate merge
-    kernel; every row against the oracle."""
+def test_attention_mixed_group_counts():
+    """One launch holding sequences of 1, 3, 9 and 20 key groups under a 24K-token configuration
+    (one CTA per group: every multi-group sequence is merged by the separate merge kernel)."""
     _attention_batch([700, 2500, 9000, 20000], [8, 3, 17, 8], 24576, "mixed")
+
+
+@pytest.mark.parametrize("L", [5000, 12000])
+def test_attention_merge_in_kernel_and_by_merge_kernel(L):
+    """Batch 1 under a 16K-token configuration (four CTAs per key group): 5 groups are merged
+    inside the attention kernel, 12 groups by the merge kernel."""
+    _attention_batch([L], [8], 16384, f"merge{L}")
 
 
 def _attention_batch(lens, S, max_context, tag):
