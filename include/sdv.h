@@ -77,7 +77,8 @@ typedef struct {
     int max_rows;       /* rows per sdv_spec_forward call, <= 128 */
     int max_span;       /* rows per sequence per call, <= max_rows */
     int max_context;    /* tokens per sequence; page table = ceil(max_context/page_size) slots */
-    int ngram_capacity; /* history tokens kept per sequence for n-gram lookup (0: none) */
+    int ngram_capacity; /* history tokens kept per sequence for n-gram lookup (0: none); needs vocab <= 2^21 */
+    int ngram_max_order; /* n-gram orders indexed per sequence, 1..6 (0: 2) */
 } sdv_cache_cfg;
 
 typedef struct {
@@ -206,9 +207,12 @@ int sdv_cache_seq_len(sdv_ctx *ctx, int32_t *d_len, void *stream);
 int sdv_page_table(sdv_ctx *ctx, int32_t *d_table, int32_t *d_n_pages, int32_t *d_free_top, void *stream);
 
 /* [TS] n-gram: append d_counts[b] tokens (d_tokens[b*stride + i]) to sequence
- * b's history and insert each completed 2-gram -> follower position into
- * that sequence's hash index (exact keys; a later insertion of the same
- * 2-gram overwrites, so lookup returns the most recent occurrence). */
+ * b's history; each new token at position p completes the contexts of the
+ * n tokens before it (n = 1..ngram_max_order), and each such context -> p
+ * goes into that order's hash index of the sequence ([TS]: one incrementally
+ * maintained index per n-gram order; exact keys; a later insertion of the
+ * same context overwrites, so lookup returns the most recent occurrence). A
+ * token outside [0, 2^21) sets SDV_ERR_DEVICE and stops the append. */
 int sdv_ngram_commit(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_counts, int B, int stride,
                      void *stream);
 
@@ -220,8 +224,18 @@ int sdv_ngram_commit(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_cou
 int sdv_gen_init(sdv_ctx *ctx, const int32_t *d_first, const int32_t *d_budget, int B, int k_init, int adaptive,
                  int k_max, void *stream);
 
+/* [CA] --ngram-min; [TS] --spec-pmin (for the n-gram drafter it scales the
+ * required match length). The n-gram drafter proposes off the longest
+ * context of n tokens, n_req <= n <= ngram_max_order, that occurred earlier in
+ * the history with a follower, where n_req = min_order + floor(pmin *
+ * (ngram_max_order - min_order) + 1/2). Defaults: min_order 2, pmin 0.
+ * min_order in [1, ngram_max_order], pmin in [0, 1], else SDV_ERR_ARG. Host
+ * state, read when sdv_propose is enqueued (so a captured graph keeps the
+ * values it was captured with). */
+int sdv_ngram_params(sdv_ctx *ctx, int min_order, float pmin);
+
 #define SDV_DRAFT_NONE 0  /* plain one-row steps (speculation off) */
-#define SDV_DRAFT_NGRAM 1 /* 2-gram prompt lookup over the sequence's history */
+#define SDV_DRAFT_NGRAM 1 /* n-gram prompt lookup over the sequence's history (sdv_ngram_params) */
 #define SDV_DRAFT_TABLE 2 /* drafts read from d_table[b*table_stride + g], g = tokens generated so far */
 
 /* Build the next verify span of every sequence from the loop state:

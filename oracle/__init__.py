@@ -29,12 +29,12 @@ pin values for these synthetic models.
 """
 from .model import DenseDecoder, SeqCache, rmsnorm, silu, rope_neox, attention_rows, argmax_lowest, round_bf16
 from .pages import PagePool, CapacityError
-from .spec import accept_greedy, ngram_propose, adapt_k
+from .spec import accept_greedy, ngram_propose, adapt_k, ngram_propose_multi, required_order, NgramIndex
 from .loop import generate, StepRecord
 from .sampling import draw_rows, perturbed, gumbel, uniforms
 
 __all__ = [
     "DenseDecoder", "SeqCache", "round_bf16", "rmsnorm", "silu", "rope_neox", "attention_rows", "argmax_lowest",
     "PagePool", "CapacityError", "accept_greedy", "ngram_propose", "adapt_k", "generate", "StepRecord",
-    "draw_rows", "perturbed", "gumbel", "uniforms",
+    "draw_rows", "perturbed", "gumbel", "uniforms", "ngram_propose_multi", "required_order", "NgramIndex",
 ]

@@ -31,7 +31,7 @@ EXPORTS = (
     "sdv_spec_forward", "sdv_spec_forward_sampled", "sdv_accept_greedy", "sdv_rewind_cache", "sdv_cache_seq_len", "sdv_page_table",
     "sdv_ngram_commit", "sdv_gen_init", "sdv_propose", "sdv_reset_seq", "sdv_get_status", "sdv_status_str",
     "sdv_op_attention", "sdv_profile_enable", "sdv_profile_read", "sdv_paged_attention_noalloc",
-    "sdv_fwd_trace", "sdv_noalloc_status",
+    "sdv_fwd_trace", "sdv_noalloc_status", "sdv_ngram_params",
 )
 PHASES = ("prepare", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm")
 # sdv_fwd_trace: stamps per CTA, CTAs per region (one region per launch of a forward)
@@ -54,7 +54,7 @@ class ModelCfg(ctypes.Structure):
 class CacheCfg(ctypes.Structure):
     _fields_ = [("page_size", ctypes.c_int), ("n_pages", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("max_rows", ctypes.c_int), ("max_span", ctypes.c_int), ("max_context", ctypes.c_int),
-                ("ngram_capacity", ctypes.c_int)]
+                ("ngram_capacity", ctypes.c_int), ("ngram_max_order", ctypes.c_int)]
 
 
 LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
@@ -95,6 +95,7 @@ def lib():
     L.sdv_page_table.argtypes = [vp, vp, vp, vp, vp]
     L.sdv_ngram_commit.argtypes = [vp, vp, vp, i32, i32, vp]
     L.sdv_gen_init.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp]
+    L.sdv_ngram_params.argtypes = [vp, i32, ctypes.c_float]
     L.sdv_propose.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp, vp, vp]
     L.sdv_reset_seq.argtypes = [vp, i32, vp]
     L.sdv_get_status.argtypes = [vp, P(ctypes.c_int32)]
@@ -177,11 +178,12 @@ class Verifier:
     """One context: borrowed weights, a KV pool and a workspace, all torch-owned."""
 
     def __init__(self, shape, weights: dict, page_size=16, n_pages=1024, max_batch=1, max_rows=32, max_span=17,
-                 max_context=4096, ngram_capacity=0, stream=None):
+                 max_context=4096, ngram_capacity=0, ngram_max_order=0, stream=None):
         import torch
         self.shape = shape
         self.mcfg = model_cfg(shape)
-        self.ccfg = CacheCfg(page_size, n_pages, max_batch, max_rows, max_span, max_context, ngram_capacity)
+        self.ccfg = CacheCfg(page_size, n_pages, max_batch, max_rows, max_span, max_context, ngram_capacity,
+                             ngram_max_order)
         self.weights = weights                       # name -> torch bf16 device tensor (kept alive)
         self.pool = torch.empty(kv_pool_bytes(self.mcfg, self.ccfg), dtype=torch.uint8, device="cuda")
         self.workspace = torch.empty(workspace_bytes(self.mcfg, self.ccfg) + 256, dtype=torch.uint8, device="cuda")
@@ -251,6 +253,9 @@ class Verifier:
     def gen_init(self, first, budget, B, k_init, adaptive, k_max, stream=None):
         _check(lib().sdv_gen_init(self.ctx, _ptr(first), _ptr(budget), B, k_init, int(adaptive), k_max,
                                   _stream(stream)), "gen_init")
+
+    def ngram_params(self, min_order, pmin=0.0):
+        _check(lib().sdv_ngram_params(self.ctx, min_order, float(pmin)), "ngram_params")
 
     def propose(self, drafter, table, table_stride, B, max_span, tokens, row_off, required, stream=None):
         _check(lib().sdv_propose(self.ctx, drafter, _ptr(table), table_stride, B, max_span, _ptr(tokens),

@@ -94,6 +94,8 @@ struct sdv_ctx {
     CUtensorMap tm_xb[4]{}, tm_ao[4]{}, tm_h[4]{};
     bool use_pdl = true;
     int gen_adaptive = 0, gen_kmax = 1;  // adaptive-K settings from sdv_gen_init
+    int ng_min = 2;                      // n-gram lookup: shortest match length and its pmin scaling
+    float ng_pmin = 0.f;
     // phase timing
     bool profiling = false;
     std::vector<cudaEvent_t> ev_pool;
@@ -148,6 +150,15 @@ enum { P_QKV = 0, P_O = 1, P_GU = 2, P_DOWN = 3, P_LM = 4 };
 constexpr int kTraceRegionCtas = 2048;
 constexpr size_t kTraceRegionWords = static_cast<size_t>(kTraceRegionCtas) * 16;
 
+// n-gram orders indexed per sequence: 1 .. ngram_max_order (0 selects 2).
+int ngram_orders(const sdv_cache_cfg &c) { return c.ngram_max_order > 0 ? c.ngram_max_order : 2; }
+
+// Required n-gram match length ([TS] --spec-pmin scales it for the n-gram drafter): linear from
+// min_order (pmin 0) to the highest indexed order (pmin 1), rounded half up.
+int ngram_required(int min_order, int max_order, float pmin) {
+    return min_order + static_cast<int>(std::floor(static_cast<double>(pmin) * (max_order - min_order) + 0.5));
+}
+
 // Carve the workspace. With ctx == nullptr only the size is computed.
 size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8_t *base, int sm_count) {
     size_t off = 0;
@@ -164,6 +175,7 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     const int qrows = kAttnRows / grp;
     const int work_cap = ceil_div(static_cast<long long>(c.n_pages) * c.page_size, kAttnGroup) + B;
     const int ng_slots = c.ngram_capacity > 0 ? next_pow2(std::max(16, 2 * c.ngram_capacity)) : 0;
+    const int ng_orders = ngram_orders(c);
     const int ss_tiles = ceil_div(H, 128);
 
     GemmPlan plans[5] = {make_plan((qdim + 2 * kvdim) / 128, ceil_div(H, 64), sm_count),
@@ -189,8 +201,8 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     s.n_work = reinterpret_cast<int *>(take(sizeof(int)));
     s.hist = reinterpret_cast<int *>(take(sizeof(int) * static_cast<size_t>(B) * std::max(0, c.ngram_capacity)));
     s.hist_len = reinterpret_cast<int *>(take(sizeof(int) * B));
-    s.ng_keys = reinterpret_cast<unsigned long long *>(take(sizeof(unsigned long long) * static_cast<size_t>(B) * ng_slots));
-    s.ng_vals = reinterpret_cast<int *>(take(sizeof(int) * static_cast<size_t>(B) * ng_slots));
+    s.ng_keys = reinterpret_cast<ulonglong2 *>(take(sizeof(ulonglong2) * static_cast<size_t>(B) * ng_orders * ng_slots));
+    s.ng_vals = reinterpret_cast<int *>(take(sizeof(int) * static_cast<size_t>(B) * ng_orders * ng_slots));
     s.cur_tok = reinterpret_cast<int *>(take(sizeof(int) * B));
     s.generated = reinterpret_cast<int *>(take(sizeof(int) * B));
     s.budget = reinterpret_cast<int *>(take(sizeof(int) * B));
@@ -204,6 +216,7 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     s.work_cap = work_cap;
     s.ngram_cap = c.ngram_capacity;
     s.ng_slots = ng_slots;
+    s.ng_orders = ng_orders;
 
     float *x = reinterpret_cast<float *>(take(sizeof(float) * kRowsCap * H));
     bf16 *xb = reinterpret_cast<bf16 *>(take(sizeof(bf16) * 2 * kRowsCap * H));        // hi, lo planes
@@ -279,6 +292,9 @@ int check_cfg(const sdv_model_cfg *m, const sdv_cache_cfg *c) {
     if (c->max_rows <= 0 || c->max_rows > kRowsCap || c->max_span <= 0 || c->max_span > c->max_rows)
         return SDV_ERR_ARG;
     if (c->max_context <= 0 || c->ngram_capacity < 0) return SDV_ERR_ARG;
+    if (c->ngram_max_order < 0 || c->ngram_max_order > kNgramMaxOrder) return SDV_ERR_ARG;
+    // n-gram contexts pack 21 bits per token
+    if (c->ngram_capacity > 0 && m->vocab > (1 << kNgramTokenBits)) return SDV_ERR_UNSUPPORTED;
     return SDV_OK;
 }
 
@@ -953,8 +969,18 @@ int sdv_propose(sdv_ctx *ctx, int drafter, const int32_t *d_table, int table_str
     if (drafter != SDV_DRAFT_NONE && drafter != SDV_DRAFT_NGRAM && drafter != SDV_DRAFT_TABLE) return SDV_ERR_ARG;
     if (drafter == SDV_DRAFT_TABLE && (!d_table || table_stride <= 0)) return SDV_ERR_ARG;
     if (drafter == SDV_DRAFT_NGRAM && ctx->c.ngram_capacity <= 0) return SDV_ERR_UNSUPPORTED;
+    const int n_max = ngram_orders(ctx->c);
+    const int ng_req = ngram_required(std::min(ctx->ng_min, n_max), n_max, ctx->ng_pmin);
     return rc(launch(ctx, propose_kernel, dim3(1), dim3(256), 0, static_cast<cudaStream_t>(stream), ctx->st, drafter,
-                     d_table, table_stride, B, max_span, d_tokens, d_row_off, d_required));
+                     d_table, table_stride, B, max_span, ng_req, d_tokens, d_row_off, d_required));
+}
+
+int sdv_ngram_params(sdv_ctx *ctx, int min_order, float pmin) {
+    if (!ctx || min_order < 1 || min_order > ngram_orders(ctx->c) || !(pmin >= 0.f && pmin <= 1.f))
+        return SDV_ERR_ARG;
+    ctx->ng_min = min_order;
+    ctx->ng_pmin = pmin;
+    return SDV_OK;
 }
 
 int sdv_reset_seq(sdv_ctx *ctx, int b, void *stream) {

@@ -26,17 +26,21 @@ struct DevState {
     // n-gram / loop state
     int *hist;          // [max_batch][ngram_cap]
     int *hist_len;      // [max_batch]
-    unsigned long long *ng_keys;  // [max_batch][ng_slots]
-    int *ng_vals;       // [max_batch][ng_slots]
+    ulonglong2 *ng_keys;  // [max_batch][ng_orders][ng_slots]: n-token context, order n = 1..ng_orders
+    int *ng_vals;         // [max_batch][ng_orders][ng_slots]: position of its most recent follower
     int *cur_tok, *generated, *budget, *kcur;  // [max_batch]
     int max_batch, pages_per_seq, page_size, n_pages_total, max_rows, max_span, work_cap;
-    int ngram_cap, ng_slots;
+    int ngram_cap, ng_slots, ng_orders;
 };
 
+// An n-gram context of up to six tokens, 21 bits each, packed exactly: tokens 0-2 in x, 3-5 in y.
+// x never has its top bit set, so an all-ones x marks an empty slot.
 constexpr unsigned long long kEmptyKey = 0xffffffffffffffffull;
+constexpr int kNgramMaxOrder = 6;
+constexpr int kNgramTokenBits = 21;
 
-__device__ __forceinline__ uint32_t ng_hash(unsigned long long key, int slots) {
-    const unsigned long long h = key * 0x9E3779B97F4A7C15ull;
+__device__ __forceinline__ uint32_t ng_hash(ulonglong2 key, int slots) {
+    const unsigned long long h = key.x * 0x9E3779B97F4A7C15ull ^ (key.y + 0x632BE59BD9B4E019ull) * 0xC2B2AE3D27D4EB4Full;
     return static_cast<uint32_t>(h >> 32) & static_cast<uint32_t>(slots - 1);
 }
 
@@ -54,8 +58,8 @@ __global__ void init_state_kernel(DevState s) {
         s.budget[i] = 0;
         s.kcur[i] = 1;
     }
-    const long long nslots = static_cast<long long>(s.max_batch) * s.ng_slots;
-    for (long long i = tid; i < nslots; i += nth) s.ng_keys[i] = kEmptyKey;
+    const long long nslots = static_cast<long long>(s.max_batch) * s.ng_orders * s.ng_slots;
+    for (long long i = tid; i < nslots; i += nth) s.ng_keys[i] = make_ulonglong2(kEmptyKey, 0ull);
     if (tid == 0) {
         *s.free_top = s.n_pages_total;
         *s.status = 0;
@@ -323,18 +327,22 @@ __global__ void reset_seq_kernel(DevState s, int b) {
         s.budget[b] = 0;
         s.kcur[b] = 1;
     }
-    for (int i = threadIdx.x; i < s.ng_slots; i += blockDim.x)
-        s.ng_keys[static_cast<size_t>(b) * s.ng_slots + i] = kEmptyKey;
+    for (int i = threadIdx.x; i < s.ng_orders * s.ng_slots; i += blockDim.x)
+        s.ng_keys[static_cast<size_t>(b) * s.ng_orders * s.ng_slots + i] = make_ulonglong2(kEmptyKey, 0ull);
 }
 
 // ------------------------------------------------------------------ n-gram index and proposer
-__device__ __forceinline__ bool ng_insert(DevState &s, int b, unsigned long long key, int val) {
-    unsigned long long *keys = s.ng_keys + static_cast<size_t>(b) * s.ng_slots;
-    int *vals = s.ng_vals + static_cast<size_t>(b) * s.ng_slots;
+__device__ __forceinline__ size_t ng_table(const DevState &s, int b, int n) {
+    return (static_cast<size_t>(b) * s.ng_orders + (n - 1)) * s.ng_slots;
+}
+
+__device__ __forceinline__ bool ng_insert(DevState &s, int b, int n, ulonglong2 key, int val) {
+    ulonglong2 *keys = s.ng_keys + ng_table(s, b, n);
+    int *vals = s.ng_vals + ng_table(s, b, n);
     uint32_t h = ng_hash(key, s.ng_slots);
     for (int probe = 0; probe < s.ng_slots; ++probe) {
-        const unsigned long long k = keys[h];
-        if (k == kEmptyKey || k == key) {
+        const ulonglong2 k = keys[h];
+        if (k.x == kEmptyKey || (k.x == key.x && k.y == key.y)) {
             keys[h] = key;
             vals[h] = val;
             return true;
@@ -344,23 +352,29 @@ __device__ __forceinline__ bool ng_insert(DevState &s, int b, unsigned long long
     return false;
 }
 
-__device__ __forceinline__ int ng_lookup(const DevState &s, int b, unsigned long long key) {
-    const unsigned long long *keys = s.ng_keys + static_cast<size_t>(b) * s.ng_slots;
-    const int *vals = s.ng_vals + static_cast<size_t>(b) * s.ng_slots;
+__device__ __forceinline__ int ng_lookup(const DevState &s, int b, int n, ulonglong2 key) {
+    const ulonglong2 *keys = s.ng_keys + ng_table(s, b, n);
+    const int *vals = s.ng_vals + ng_table(s, b, n);
     uint32_t h = ng_hash(key, s.ng_slots);
     for (int probe = 0; probe < s.ng_slots; ++probe) {
-        const unsigned long long k = keys[h];
-        if (k == key) return vals[h];
-        if (k == kEmptyKey) return -1;
+        const ulonglong2 k = keys[h];
+        if (k.x == key.x && k.y == key.y) return vals[h];
+        if (k.x == kEmptyKey) return -1;
         h = (h + 1) & static_cast<uint32_t>(s.ng_slots - 1);
     }
     return -1;
 }
 
-__device__ __forceinline__ unsigned long long ng_key(int t1, int t2) {
-    return (static_cast<unsigned long long>(static_cast<uint32_t>(t1)) << 32) | static_cast<uint32_t>(t2);
+// The context h[end - n .. end - 1] as a packed key.
+__device__ __forceinline__ ulonglong2 ng_key(const int *h, int end, int n) {
+    unsigned long long w[2] = {0ull, 0ull};
+    for (int i = 0; i < n; ++i)
+        w[i / 3] |= static_cast<unsigned long long>(static_cast<uint32_t>(h[end - n + i])) << (kNgramTokenBits * (i % 3));
+    return make_ulonglong2(w[0], w[1]);
 }
 
+// Append tokens to sequence b's history; each new token at position L completes the contexts
+// h[L-n .. L-1] (n = 1 .. orders), which now map to L, their most recent follower.
 __global__ void ngram_commit_kernel(DevState s, const int *tokens, const int *counts, int B, int stride) {
     pdl_trigger();
     pdl_wait();
@@ -374,8 +388,14 @@ __global__ void ngram_commit_kernel(DevState s, const int *tokens, const int *co
             set_status(s.status, SDV_ERR_CAPACITY);
             break;
         }
-        h[L] = tokens[static_cast<size_t>(b) * stride + i];
-        if (L >= 2 && !ng_insert(s, b, ng_key(h[L - 2], h[L - 1]), L)) set_status(s.status, SDV_ERR_CAPACITY);
+        const int tok = tokens[static_cast<size_t>(b) * stride + i];
+        if (tok < 0 || tok >= (1 << kNgramTokenBits)) {
+            set_status(s.status, SDV_ERR_DEVICE);
+            break;
+        }
+        for (int o = 1; o <= s.ng_orders && o <= L; ++o)
+            if (!ng_insert(s, b, o, ng_key(h, L, o), L)) set_status(s.status, SDV_ERR_CAPACITY);
+        h[L] = tok;
         ++L;
     }
     s.hist_len[b] = L;
@@ -393,8 +413,10 @@ __global__ void gen_init_kernel(DevState s, const int *first, const int *budget,
 }
 
 // One block; thread b builds sequence b's span, thread 0 packs the offsets.
+// n-gram drafter: the longest order n in [ng_req, ng_orders] whose last-n-token context occurred
+// earlier with a follower; its most recent occurrence gives up to k drafts.
 __global__ void propose_kernel(DevState s, int drafter, const int *table, int table_stride, int B, int max_span,
-                               int *tokens, int *row_off, int *required) {
+                               int ng_req, int *tokens, int *row_off, int *required) {
     pdl_trigger();
     pdl_wait();
     __shared__ int len_s[257], off_s[257];
@@ -409,12 +431,14 @@ __global__ void propose_kernel(DevState s, int drafter, const int *table, int ta
             k = min(k, max_span - 1);
             if (drafter == SDV_DRAFT_NGRAM && k > 0 && s.ngram_cap > 0) {
                 const int L = s.hist_len[b];
-                if (L >= 3) {
-                    const int *h = s.hist + static_cast<size_t>(b) * s.ngram_cap;
-                    const int j = ng_lookup(s, b, ng_key(h[L - 2], h[L - 1]));
-                    if (j >= 2 && j < L) {
+                const int *h = s.hist + static_cast<size_t>(b) * s.ngram_cap;
+                for (int o = s.ng_orders; o >= ng_req && o >= 1; --o) {
+                    if (L < o + 1) continue;
+                    const int j = ng_lookup(s, b, o, ng_key(h, L, o));
+                    if (j >= o && j < L) {
                         src = j;
                         n = min(k, L - j);
+                        break;
                     }
                 }
             } else if (drafter == SDV_DRAFT_TABLE && k > 0) {

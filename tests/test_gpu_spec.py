@@ -64,6 +64,37 @@ def test_ngram_proposer_matches_oracle(tiny):
     assert v.get_status() == 0
 
 
+@pytest.mark.parametrize("n_max,n_min,pmin", [(6, 2, 0.0), (6, 2, 0.5), (4, 1, 0.0), (3, 3, 0.0), (5, 2, 1.0)])
+def test_multi_order_ngram_proposer_matches_oracle(tiny, n_max, n_min, pmin):
+    """[TS] one index per n-gram order and --spec-pmin scaling the required match length; [CA]
+    --ngram-min: the device's longest-match lookup against the oracle's backward scan, at every
+    prefix of repeat-heavy histories over a small alphabet."""
+    import torch
+    from speculative_decoding_verify_02_gb300 import SDV_DRAFT_NGRAM
+    _, dev, _ = tiny
+    B, V = 4, 6
+    hists = [list(map(int, workloads.span_repeat_prompt(60 + b, n_spans=14, span=6, vocab=V))) for b in range(B)]
+    v = _verifier(dev, max_batch=B, ngram_max_order=n_max)
+    v.ngram_params(n_min, pmin)
+    max_span = 8
+    toks, ro, req = _t(np.zeros(B * max_span)), _t(np.zeros(B + 1)), _t(np.zeros(B))
+    hit = 0
+    for n in range(1, len(hists[0]) + 1):
+        v.ngram_commit(_t([h[n - 1] for h in hists]), _t([1] * B), B, 1)
+        k = 1 + n % 7
+        v.gen_init(_t([h[n - 1] for h in hists]), _t([10_000] * B), B, k, False, 7)
+        v.propose(SDV_DRAFT_NGRAM, None, 0, B, max_span, toks, ro, req)
+        torch.cuda.synchronize()
+        t, o = toks.cpu().numpy(), ro.cpu().numpy()
+        for b in range(B):
+            d = oracle.ngram_propose_multi(hists[b][:n], k, n_min, n_max, pmin)
+            hit += bool(d)
+            assert t[o[b]:o[b + 1]].tolist() == [hists[b][n - 1]] + d, (n, b)
+    assert v.get_status() == 0
+    assert hit > 0
+    v.close()
+
+
 def test_adaptive_k_trajectory(tiny):
     """[CA] adaptive K inside accept_greedy, read back through the proposer's
     span lengths (table drafter), against the oracle's rule on scripted rounds."""

@@ -9,6 +9,7 @@ import os
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from oracle import CapacityError, DenseDecoder, PagePool, accept_greedy, adapt_k, generate, ngram_propose
 from synth import workloads
@@ -215,3 +216,48 @@ def test_oracle_reproduces_its_recorded_ngram_k4_run(tiny_model):
     for r, row in zip(rec, rows[1:]):
         assert r.spans[0] == _ints(row[1]) and r.argmax[0] == _ints(row[2])
         assert r.m[0] == int(row[3]) and r.new_len[0] == int(row[4])
+
+
+# ----------------------------------------------------------------------------- multi-order n-gram
+
+def test_required_order_reading():
+    """[TS] "--spec-pmin" scales the n-gram drafter's required match length; [CA] "--ngram-min 2".
+    Reading: linear from n_min (pmin 0) to n_max (pmin 1), rounded half up."""
+    assert [oracle.required_order(2, 6, p) for p in (0.0, 0.25, 0.5, 0.75, 1.0)] == [2, 3, 4, 5, 6]
+    assert [oracle.required_order(1, 4, p) for p in (0.0, 0.1, 0.2, 0.5, 0.9, 1.0)] == [1, 1, 2, 3, 4, 4]
+    assert oracle.required_order(3, 3, 0.7) == 3
+
+
+def test_multi_order_prefers_the_longest_match():
+    h = [5, 3, 4, 8, 2, 3, 4, 9, 6, 5, 3, 4]
+    assert oracle.ngram_propose(h, 2, 2) == [9, 6]                    # most recent 2-gram [3, 4]
+    assert oracle.ngram_propose_multi(h, 2, 2, 3) == [8, 2]          # the 3-gram [5, 3, 4] wins
+    assert oracle.ngram_propose_multi(h, 2, 2, 3, pmin=1.0) == [8, 2]
+    assert oracle.ngram_propose_multi(h, 2, 2, 4, pmin=1.0) == []    # no 4-token context repeats
+    assert oracle.ngram_propose_multi(h, 2, 3, 3) == [8, 2]
+    assert oracle.ngram_propose_multi(h, 0, 2, 3) == []
+
+
+@pytest.mark.parametrize("vocab", [3, 6, 40])
+def test_multi_order_index_matches_brute_force(vocab):
+    """The incremental per-order index against the backward scan at every prefix of random and
+    repeat-heavy histories, for several (n_min, n_max, pmin); with n_min = n_max = 2 both reduce to
+    the 2-gram proposer."""
+    rng = np.random.default_rng(vocab)
+    hists = [rng.integers(0, vocab, 160).tolist(),
+             list(map(int, workloads.span_repeat_prompt(vocab, n_spans=20, span=8, vocab=vocab)))]
+    for h in hists:
+        for n_min, n_max, pmin in ((2, 2, 0.0), (1, 4, 0.0), (2, 6, 0.5), (2, 5, 1.0), (3, 6, 0.3)):
+            idx = oracle.NgramIndex(n_max)
+            for L, t in enumerate(h):
+                idx.append(t)
+                k = 1 + (L % 7)
+                brute = oracle.ngram_propose_multi(h[:L + 1], k, n_min, n_max, pmin)
+                assert idx.propose(k, n_min, pmin) == brute, (L, n_min, n_max, pmin)
+                if (n_min, n_max) == (2, 2):
+                    assert brute == oracle.ngram_propose(h[:L + 1], k, 2)
+                if brute:   # the drafts follow an earlier occurrence of at least n_req context tokens
+                    n_req = oracle.required_order(n_min, n_max, pmin)
+                    ctx = h[L + 1 - n_req:L + 1]
+                    assert any(h[j - n_req:j] == ctx and h[j:j + len(brute)] == brute
+                               for j in range(n_req, L + 1))
