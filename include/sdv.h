@@ -340,6 +340,53 @@ int sdv_paged_attention_noalloc(const void *d_q, const void *d_kv_layer, const i
  * clear it. Allocates nothing. The pages have no counterpart of this call. */
 int sdv_noalloc_status(int32_t *h_status);
 
+/* Speculation cost governor ([TS] SpeculationCostGovernor and the paragraphs on
+ * the shared governor): a host-side policy, one per (model, drafter, device),
+ * that decides before each step whether it drafts, from the measured time of
+ * earlier steps; no GPU work. Rules: verdicts compare ms per committed token of
+ * speculative steps with the plain baseline (the mean over the last
+ * baseline_samples plain samples); a probe is probe_steps speculative steps,
+ * after a loss reprobe_steps; a loss parks drafting for first_park tokens,
+ * doubling per further loss up to max_park, and a win resets that; a probe
+ * ends early, lost, after zero_accept_end speculative steps in a row accepted
+ * nothing; while a win holds, the governor parks as soon as the last
+ * hold_window speculative steps average a loss, and re-measures the baseline
+ * with remeasure_steps plain steps every remeasure_every speculative steps; a
+ * speculative step that proposed nothing counts as one token; parked steps
+ * feed the baseline except the first; the governor starts with remeasure_steps
+ * plain calibration steps. */
+typedef struct sdv_governor sdv_governor; /* opaque host state */
+typedef struct {
+    int probe_steps;      /* 8 */
+    int reprobe_steps;    /* 3 */
+    int first_park;       /* 32 tokens */
+    int max_park;         /* 256 tokens */
+    int hold_window;      /* 8 */
+    int remeasure_every;  /* 64 */
+    int remeasure_steps;  /* 3 */
+    int zero_accept_end;  /* 4 */
+    int baseline_samples; /* 64 */
+} sdv_governor_cfg;
+typedef struct {
+    float plain_ms_per_tok; /* the baseline, or -1 before any plain sample */
+    float spec_ms_per_tok;  /* over every speculative sample, or -1 */
+    int wins, losses, parked_steps;
+    int state;              /* 0 calibrate, 1 probe, 2 hold, 3 re-measure, 4 parked */
+} sdv_governor_report;
+
+/* cfg NULL: the values above. Values < 1, or max_park < first_park: SDV_ERR_ARG. */
+int sdv_governor_create(const sdv_governor_cfg *cfg, sdv_governor **out);
+int sdv_governor_destroy(sdv_governor *g);
+/* *h_speculate = 1 if the next step drafts, 0 for a plain one-row step. */
+int sdv_governor_decide(sdv_governor *g, int32_t *h_speculate);
+/* The finished step: whether it drafted, its device time, tokens committed
+ * (summed over the batch), drafts proposed and accepted. */
+int sdv_governor_record(sdv_governor *g, int speculative, float ms, int committed, int drafted, int accepted);
+/* A new request: the park left is capped at first_park and the backoff is
+ * forgotten; a loss already recorded keeps the next probe short. */
+int sdv_governor_new_request(sdv_governor *g);
+int sdv_governor_stats(sdv_governor *g, sdv_governor_report *out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,7 +31,8 @@ EXPORTS = (
     "sdv_spec_forward", "sdv_spec_forward_sampled", "sdv_accept_greedy", "sdv_rewind_cache", "sdv_cache_seq_len", "sdv_page_table",
     "sdv_ngram_commit", "sdv_gen_init", "sdv_propose", "sdv_reset_seq", "sdv_get_status", "sdv_status_str",
     "sdv_op_attention", "sdv_profile_enable", "sdv_profile_read", "sdv_paged_attention_noalloc",
-    "sdv_fwd_trace", "sdv_noalloc_status", "sdv_ngram_params",
+    "sdv_fwd_trace", "sdv_noalloc_status", "sdv_ngram_params", "sdv_governor_create", "sdv_governor_destroy",
+    "sdv_governor_decide", "sdv_governor_record", "sdv_governor_new_request", "sdv_governor_stats",
 )
 PHASES = ("prepare", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm")
 # sdv_fwd_trace: stamps per CTA, CTAs per region (one region per launch of a forward)
@@ -55,6 +56,17 @@ class CacheCfg(ctypes.Structure):
     _fields_ = [("page_size", ctypes.c_int), ("n_pages", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("max_rows", ctypes.c_int), ("max_span", ctypes.c_int), ("max_context", ctypes.c_int),
                 ("ngram_capacity", ctypes.c_int), ("ngram_max_order", ctypes.c_int)]
+
+
+class GovernorCfg(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("probe_steps", "reprobe_steps", "first_park", "max_park", "hold_window",
+                                              "remeasure_every", "remeasure_steps", "zero_accept_end",
+                                              "baseline_samples")]
+
+
+class GovernorStats(ctypes.Structure):
+    _fields_ = [("plain_ms_per_tok", ctypes.c_float), ("spec_ms_per_tok", ctypes.c_float), ("wins", ctypes.c_int),
+                ("losses", ctypes.c_int), ("parked_steps", ctypes.c_int), ("state", ctypes.c_int)]
 
 
 LAYER_FIELDS = ("attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
@@ -96,6 +108,12 @@ def lib():
     L.sdv_ngram_commit.argtypes = [vp, vp, vp, i32, i32, vp]
     L.sdv_gen_init.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp]
     L.sdv_ngram_params.argtypes = [vp, i32, ctypes.c_float]
+    L.sdv_governor_create.argtypes = [P(GovernorCfg), P(vp)]
+    L.sdv_governor_destroy.argtypes = [vp]
+    L.sdv_governor_decide.argtypes = [vp, P(ctypes.c_int32)]
+    L.sdv_governor_record.argtypes = [vp, i32, ctypes.c_float, i32, i32, i32]
+    L.sdv_governor_new_request.argtypes = [vp]
+    L.sdv_governor_stats.argtypes = [vp, P(GovernorStats)]
     L.sdv_propose.argtypes = [vp, i32, vp, i32, i32, i32, vp, vp, vp, vp]
     L.sdv_reset_seq.argtypes = [vp, i32, vp]
     L.sdv_get_status.argtypes = [vp, P(ctypes.c_int32)]
@@ -172,6 +190,48 @@ def upload_bf16(bits: np.ndarray, device="cuda"):
     import torch
     t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
     return t.to(device).view(torch.bfloat16)
+
+
+class Governor:
+    """The speculation cost governor (host policy in the library): decide() before a step,
+    record() after it."""
+    STATES = ("calibrate", "probe", "hold", "remeasure", "parked")
+
+    def __init__(self, cfg: GovernorCfg = None):
+        g = ctypes.c_void_p()
+        _check(lib().sdv_governor_create(ctypes.byref(cfg) if cfg is not None else None, ctypes.byref(g)),
+               "governor_create")
+        self.g = g
+
+    def decide(self) -> bool:
+        v = ctypes.c_int32()
+        _check(lib().sdv_governor_decide(self.g, ctypes.byref(v)), "governor_decide")
+        return bool(v.value)
+
+    def record(self, speculative: bool, ms: float, committed: int, drafted: int, accepted: int):
+        _check(lib().sdv_governor_record(self.g, int(speculative), float(ms), int(committed), int(drafted),
+                                         int(accepted)), "governor_record")
+
+    def new_request(self):
+        _check(lib().sdv_governor_new_request(self.g), "governor_new_request")
+
+    def stats(self) -> dict:
+        s = GovernorStats()
+        _check(lib().sdv_governor_stats(self.g, ctypes.byref(s)), "governor_stats")
+        return {"plain_ms_per_tok": None if s.plain_ms_per_tok < 0 else s.plain_ms_per_tok,
+                "spec_ms_per_tok": None if s.spec_ms_per_tok < 0 else s.spec_ms_per_tok,
+                "wins": s.wins, "losses": s.losses, "parked": s.parked_steps, "state": self.STATES[s.state]}
+
+    def close(self):
+        if self.g:
+            lib().sdv_governor_destroy(self.g)
+            self.g = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class Verifier:

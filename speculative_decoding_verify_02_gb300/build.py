@@ -5,7 +5,8 @@ import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
-SRC = [os.path.join(PKG, "csrc", "sdv_api.cu"), os.path.join(PKG, "csrc", "noalloc.cu")]
+SRC = [os.path.join(PKG, "csrc", "sdv_api.cu"), os.path.join(PKG, "csrc", "noalloc.cu"),
+       os.path.join(PKG, "csrc", "governor.cpp")]
 DEPS = [os.path.join(PKG, "csrc", f) for f in os.listdir(os.path.join(PKG, "csrc"))] + \
        [os.path.join(ROOT, "include", "sdv.h")]
 LIB = os.path.join(PKG, "libsdv.so")

@@ -3,8 +3,9 @@
 Nothing here computes a step of the method: it only orders the library calls
 (prefill chunks, then per step propose -> ensure_capacity -> spec_forward ->
 accept_greedy -> rewind_cache -> ngram_commit), owns the device buffers those
-calls read and write, and can capture one step as a CUDA graph so that a step
-costs one launch. Every length the kernels need stays in device memory, so a
+calls read and write, can capture one step as a CUDA graph so that a step
+costs one launch, and can let the library's speculation cost governor decide
+each step. Every length the kernels need stays in device memory, so a
 captured step replays correctly whatever the spans and cache lengths are.
 """
 from __future__ import annotations
@@ -113,6 +114,30 @@ class SpecLoop:
         v.rewind_cache(self.new_len, B)
         if ngram:
             v.ngram_commit(self.committed, self.n_commit, B, self.max_span)
+
+    def governed_step(self, governor, drafter=SDV_DRAFT_NGRAM, **kw):
+        """One step under the speculation cost governor: it decides whether this step drafts (else
+        a plain one-row step through the same calls), the step's device time is measured with CUDA
+        events, and the governor records it with the tokens committed, drafted and accepted over
+        the batch. Returns (speculated, committed tokens, ms). Synchronises once per step."""
+        import torch
+        spec = governor.decide()
+        s = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        self.step(drafter=drafter if spec else SDV_DRAFT_NONE, **kw)
+        e1.record(s)
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        n_commit = self.n_commit.cpu().numpy()
+        n_accept = self.n_accept.cpu().numpy()
+        spans = np.diff(self.row_off.cpu().numpy())
+        committed = int(n_commit.sum())
+        drafted = int(np.clip(spans - 1, 0, None).sum())
+        accepted = int(np.clip(n_accept, 0, None).sum())
+        if committed > 0:  # a step after every budget is met is not a sample
+            governor.record(spec, ms, committed, drafted, accepted)
+        return spec, committed, ms
 
     def capture(self, **kw):
         """Capture one step as a CUDA graph (replayed by replay())."""

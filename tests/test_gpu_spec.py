@@ -190,6 +190,41 @@ def test_ngram_loop_spec_on_equals_spec_off(tiny):
     assert on == off and len(on[0]) == 32
 
 
+def test_governed_loop_is_lossless(tiny):
+    """[TS] the cost governor parks and re-probes drafting by measured step time; whatever it
+    decides, every emitted token is drawn from a trunk row, so the governed n-gram loop emits the
+    plain loop's stream. The governor sees real step times and samples."""
+    import speculative_decoding_verify_02_gb300 as sdv
+    from speculative_decoding_verify_02_gb300.runner import SpecLoop
+    _, dev, _ = tiny
+    prompts = [workloads.motif_prompt(1), synth.tokens(8, "gov.p2", 57, synth.TINY.vocab)]
+    B, budget = 2, [40, 40]
+    plain = _run_loop(_verifier(dev, max_batch=B), B, prompts, budget, 0, 0)
+    v = _verifier(dev, max_batch=B)
+    loop = SpecLoop(v, B, 8)
+    first = loop.prefill(prompts, ngram=True)
+    loop.start(budget, k_init=1, adaptive=True, k_max=7)
+    gov = sdv.Governor(sdv.GovernorCfg(4, 2, 4, 16, 4, 8, 2, 3, 16))      # short intervals: every state
+    streams = [[int(f)] for f in first]
+    decisions = []
+    for _ in range(200):
+        spec, committed, ms = loop.governed_step(gov, drafter=sdv.SDV_DRAFT_NGRAM, ngram=True)
+        nc, cm = loop.n_commit.cpu().numpy(), loop.committed.cpu().numpy().reshape(B, 8)
+        for b in range(B):
+            streams[b] += cm[b, :nc[b]].tolist()
+        decisions.append(spec)
+        if all(len(s) >= bb for s, bb in zip(streams, budget)):
+            break
+    assert v.get_status() == 0
+    assert streams == plain
+    st = gov.stats()
+    assert st["plain_ms_per_tok"] and st["spec_ms_per_tok"] and st["wins"] + st["losses"] >= 1
+    assert any(decisions) and not all(decisions)
+    print("governor:", st)
+    gov.close()
+    v.close()
+
+
 def test_error_paths_report_and_leave_state(tiny):
     """Failures are reported through the status word and leave the state as it was:
     the pool running dry, a request past the page table, a rewind past the written
