@@ -65,6 +65,13 @@ typedef struct {
     int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
     float rms_eps, rope_theta;
     int qk_norm; /* 1: per-head RMSNorm on q and k before RoPE */
+    /* [TS] sliding-window caches: with swa_window > 0, layer l is a local layer
+     * (its row at position q attends positions q - swa_window + 1 .. q) unless
+     * swa_global_every > 0 and (l + 1) % swa_global_every == 0. A local layer
+     * keeps exactly one window of positions in a ring (position p in slot
+     * p % swa_window, on the sequence's first swa_window / page_size pages).
+     * swa_window must be a multiple of page_size and at least max_span. */
+    int swa_window, swa_global_every;
 } sdv_model_cfg;
 
 /* Cache and call limits. Attention takes its TMA-fed path when page_size is
@@ -195,7 +202,13 @@ int sdv_accept_greedy(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_ro
  * changes). Rows past it stay in the pages as stale data that nothing reads.
  * Pages past ceil(length / page_size) go back to the free stack for
  * b = B-1 down to 0, highest slot first, so a rewind to the lengths before an
- * sdv_ensure_capacity restores the pool exactly. */
+ * sdv_ensure_capacity restores the pool exactly.
+ * Sliding-window layers ([TS] sliding-window caches and rollback): the last
+ * forward kept what its rows evicted from each local layer's ring; rows of
+ * that forward at or past the new length are rejected, and their slots get
+ * back the positions they held (a full acceptance restores nothing). A rewind
+ * below the start of the last forward's span, once a ring has wrapped, would
+ * need positions no longer kept: SDV_ERR_ARG, nothing changes. */
 int sdv_rewind_cache(sdv_ctx *ctx, const int32_t *d_length, int B, void *stream);
 
 /* [TS] CacheSeqLen: copy the max_batch cache lengths into d_len. */

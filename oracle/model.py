@@ -68,13 +68,16 @@ def rope_neox(u: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
     return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
 
 
-def attention_rows(q: np.ndarray, K: np.ndarray, V: np.ndarray, q_pos: np.ndarray, scale: float) -> np.ndarray:
+def attention_rows(q: np.ndarray, K: np.ndarray, V: np.ndarray, q_pos: np.ndarray, scale: float,
+                   window: int = 0) -> np.ndarray:
     """Causal grouped-query attention of query rows against one sequence's cache.
 
     q: [S, nq, D]; K, V: [T, nkv, D] (positions 0..T-1); q_pos[i] is row i's
     absolute position, and row i attends keys 0..q_pos[i] (the cache prefix
     plus the span rows up to and including itself). q head h reads kv head
-    h // (nq / nkv).
+    h // (nq / nkv). With window > 0 (a sliding-window layer, [TS] sliding-window
+    caches: a local layer keeps exactly one window of positions) row i attends
+    only the last `window` positions, max(0, q_pos[i] - window + 1)..q_pos[i].
     """
     S, nq, D = q.shape
     nkv = K.shape[1]
@@ -82,12 +85,13 @@ def attention_rows(q: np.ndarray, K: np.ndarray, V: np.ndarray, q_pos: np.ndarra
     out = np.empty((S, nq, D), dtype=np.float64)
     for i in range(S):
         n = int(q_pos[i]) + 1
+        lo = max(0, n - window) if window > 0 else 0
         qi = q[i].reshape(nkv, grp, D)                       # [g, r, D]
-        s = np.einsum("grd,tgd->grt", qi, K[:n]) * scale     # [g, r, n]
+        s = np.einsum("grd,tgd->grt", qi, K[lo:n]) * scale   # [g, r, n - lo]
         s = s - s.max(axis=-1, keepdims=True)
         p = np.exp(s)
         p = p / p.sum(axis=-1, keepdims=True)
-        out[i] = np.einsum("grt,tgd->grd", p, V[:n]).reshape(nq, D)
+        out[i] = np.einsum("grt,tgd->grd", p, V[lo:n]).reshape(nq, D)
     return out
 
 
@@ -187,7 +191,7 @@ class DenseDecoder:
                     continue
                 L0, r0 = caches[b].length, starts[b]
                 o[r0:r0 + c] = attention_rows(q[r0:r0 + c], caches[b].K[l][:L0 + c], caches[b].V[l][:L0 + c],
-                                              pos[r0:r0 + c], scale)
+                                              pos[r0:r0 + c], scale, sh.swa_window if sh.is_local(l) else 0)
             x = x + o.reshape(R, nq * D) @ self.w(p + "wo").T
             hb = rmsnorm(x, self.w(p + "ffn_norm"), eps)
             f = silu(hb @ self.w(p + "w_gate").T) * (hb @ self.w(p + "w_up").T)

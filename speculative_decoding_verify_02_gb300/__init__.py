@@ -49,7 +49,7 @@ class ModelCfg(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("n_q_heads", ctypes.c_int),
                 ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int),
                 ("vocab", ctypes.c_int), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
-                ("qk_norm", ctypes.c_int)]
+                ("qk_norm", ctypes.c_int), ("swa_window", ctypes.c_int), ("swa_global_every", ctypes.c_int)]
 
 
 class CacheCfg(ctypes.Structure):
@@ -143,7 +143,8 @@ def _check(code: int, what: str):
 
 def model_cfg(shape) -> ModelCfg:
     return ModelCfg(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn,
-                    shape.vocab, shape.rms_eps, shape.rope_theta, 1 if shape.qk_norm else 0)
+                    shape.vocab, shape.rms_eps, shape.rope_theta, 1 if shape.qk_norm else 0,
+                    getattr(shape, "swa_window", 0), getattr(shape, "swa_global_every", 0))
 
 
 def workspace_bytes(mcfg: ModelCfg, ccfg: CacheCfg) -> int:

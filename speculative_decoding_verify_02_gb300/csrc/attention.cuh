@@ -44,6 +44,9 @@ struct AttnArgs {
     int layer;               // attention_group.cuh: layer index in the pool tensor map
     int merge_groups;        // attention_group.cuh: sequences of up to this many key groups are merged
                              // inside the attention kernel; longer ones by attn_merge_kernel
+    int window;              // attention_group.cuh: > 0 on a sliding-window layer (ring of `window` positions)
+    int max_span;            // rows per sequence held by swa_backup
+    const bf16 *swa_backup;  // the layer's copies of the ring slots the span overwrote [max_batch][max_span][K|V][nkv][D]
     unsigned long long *trace;  // attention_group.cuh: optional [CTA][8] %globaltimer stamps, or nullptr
 };
 

@@ -111,7 +111,11 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     const int g0 = grp_idx * kAttnGroup, g1 = min(g0 + kAttnGroup, key_end);
     const int n_ch_group = (g1 - g0 + kAttnChunk - 1) / kAttnChunk;
     const int c_per = kGrpChunks / a.splits;
-    const int c_lo = sp * c_per, c_hi = min(c_lo + c_per, n_ch_group);  // this CTA's chunks (may be none)
+    // this CTA's chunks (may be none); on a sliding-window layer the chunks below every span row's
+    // window are skipped (all their keys are masked, so they would leave the state unchanged)
+    const int win_lo = a.window > 0 ? max(0, L - a.window + 1) : 0;
+    const int c_lo = max(sp * c_per, a.window > 0 ? (win_lo - g0) / kAttnChunk : 0);
+    const int c_hi = min(sp * c_per + c_per, n_ch_group);
     const int n_ch = max(0, c_hi - c_lo);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool consumer = tid < kGrpConsumers;
@@ -146,7 +150,9 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
             const int s_first = k0 / a.page_size, s_last = (k1 - 1) / a.page_size;  // page-table slots
             int page = -1;
             const int si = s_first + lane;
-            if (si <= s_last && si < a.pages_per_seq) page = a.page_table[static_cast<size_t>(b) * a.pages_per_seq + si];
+            // a sliding-window layer's positions live in a ring over the first window / page_size slots
+            const int ts = a.window > 0 ? si % (a.window / a.page_size) : si;
+            if (si <= s_last && ts < a.pages_per_seq) page = a.page_table[static_cast<size_t>(b) * a.pages_per_seq + ts];
             const bool ok = page >= 0 && page < a.n_pages;
             if (si <= s_last && !ok) set_status(a.status, SDV_ERR_CAPACITY);
             const int bytes = __reduce_add_sync(0xffffffffu, ok ? box_bytes : 0);
@@ -195,10 +201,24 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         const uint32_t sKV = smem_u32(sm + S::BUF_OFF + buf * 2 * S::KV_BYTES);
         {   // keys past the group end read as zero V rows (the pool holds stale data there)
             const int kstart = g0 + (c_lo + ch) * kAttnChunk, nvalid = min(kAttnChunk, g1 - kstart);
-            if (nvalid < kAttnChunk) {  // the same for every consumer warp
+            // sliding-window layer: the span rows overwrote the ring slots of positions
+            // L - window .. L + S_b - 1 - window; those still in a row's window are read from the
+            // layer's backup instead (span row j kept position L + j - window)
+            const int ev_lo = max(kstart, max(win_lo, L - a.window)), ev_hi = min(kstart + nvalid, L + S_b - a.window);
+            const int n_ev = a.window > 0 ? max(0, ev_hi - ev_lo) : 0;
+            if (nvalid < kAttnChunk || n_ev > 0) {  // the same for every consumer warp
                 for (int e = tid; e < (kAttnChunk - nvalid) * CH; e += kGrpConsumers) {
                     const int r = nvalid + e / CH, c = e % CH;
                     asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(sKV + swz_kv<D>(r, c, 1, lp)), "r"(0u) : "memory");
+                }
+                for (int e = tid; e < n_ev * 2 * CH; e += kGrpConsumers) {
+                    const int u = ev_lo + e / (2 * CH), kv = (e / CH) & 1, c = e % CH;
+                    const int j = u - (L - a.window);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                        a.swa_backup + ((static_cast<size_t>(b) * a.max_span + j) * 2 + kv) * a.nkv * D + g * D + c * 8);
+                    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sKV + swz_kv<D>(u - kstart, c, kv, lp)),
+                                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                 : "memory");
                 }
                 named_bar_sync(1, kGrpConsumers);
             }
@@ -247,7 +267,11 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int u = ubase + nt * 8 + tq * 2 + e;
-                    const bool ok0 = u < g1 && u <= lim0, ok1 = u < g1 && u <= lim1;
+                    bool ok0 = u < g1 && u <= lim0, ok1 = u < g1 && u <= lim1;
+                    if (a.window > 0) {  // sliding window: the row's last `window` positions
+                        ok0 = ok0 && u > lim0 - a.window;
+                        ok1 = ok1 && u > lim1 - a.window;
+                    }
                     s[nt][e] = ok0 ? s[nt][e] * a.scale_log2 : -INFINITY;
                     s[nt][2 + e] = ok1 ? s[nt][2 + e] * a.scale_log2 : -INFINITY;
                     mx0 = fmaxf(mx0, s[nt][e]);

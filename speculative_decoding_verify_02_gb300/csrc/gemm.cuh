@@ -47,6 +47,11 @@ struct GemmArgs {
     const int *row_seq, *row_pos, *page_table;
     int pages_per_seq, page_size, n_pages;
     bf16 *q_out, *kv_layer;            // q_out: [2 planes][rows_cap][nq][D]
+    // sliding-window layer: ring size, the layer's backup of the slots a span overwrites
+    // ([max_batch][max_span][K|V][nkv][D]), the sequences' lengths before the span
+    int swa_window, max_span;
+    bf16 *swa_backup;
+    const int *seq_base;
     // residual epilogue
     float *x;
     bf16 *xb;                          // [2 planes][rows_cap][hidden]
@@ -130,7 +135,7 @@ struct EpiLayer {
 // (cos, sin) pairs of the lane's features and, for K and V tiles, the page holding the position.
 // Loaded while the MMAs run, so the row's finish does not wait on global memory.
 struct QkvRow {
-    int pos, page;
+    int pos, page, span_row;  // span_row: the row's index in its sequence's span (sliding-window backup)
     float2 c0, c1;
 };
 
@@ -163,10 +168,15 @@ __device__ __forceinline__ QkvRow qkv_row_load(const GemmArgs &a, int tile, int 
             q.c0 = a.rope[static_cast<size_t>(p) * 32 + lane];
         }
     }
+    q.span_row = -1;
     if (section > 0) {
-        const int seq = a.row_seq[r], slot_idx = q.pos / a.page_size;
+        // a sliding-window layer keeps one window of positions in a ring: position p in slot
+        // p % window, whose pages are the sequence's first window / page_size page-table entries
+        const int seq = a.row_seq[r];
+        const int slot_idx = (a.swa_window > 0 ? q.pos % a.swa_window : q.pos) / a.page_size;
         if (seq >= 0 && q.pos >= 0 && slot_idx < a.pages_per_seq)
             q.page = a.page_table[static_cast<size_t>(seq) * a.pages_per_seq + slot_idx];
+        if (a.swa_backup != nullptr && seq >= 0) q.span_row = q.pos - a.seq_base[seq];
     }
     return q;
 }
@@ -238,12 +248,19 @@ __device__ __forceinline__ void epi_qkv_core(const GemmArgs &a, const EpiLayer &
         if (lane == 0) set_status(a.status, SDV_ERR_CAPACITY);
         return;
     }
+    // sliding-window layer: the slot about to be written holds position pos - window, which other
+    // rows of this span may still attend and a rejection must give back; keep it first
+    bf16 *keep = nullptr;
+    if (a.swa_backup != nullptr && q.span_row >= 0 && q.span_row < a.max_span)
+        keep = a.swa_backup + ((static_cast<size_t>(a.row_seq[r]) * a.max_span + q.span_row) * 2 + (section - 1)) *
+                                  a.nkv * D;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int fs = fbase + lane + 32 * i;
         const size_t off =
             (((static_cast<size_t>(page) * 2 + (section - 1)) * a.nkv + fs / D) * a.page_size + pos % a.page_size) * D +
             fs % D;
+        if (keep != nullptr) keep[fs] = el.kv_layer[off];
         el.kv_layer[off] = __float2bfloat16(x[i]);
     }
 }

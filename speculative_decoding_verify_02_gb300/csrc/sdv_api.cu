@@ -94,6 +94,9 @@ struct sdv_ctx {
     CUtensorMap tm_xb[4]{}, tm_ao[4]{}, tm_h[4]{};
     bool use_pdl = true;
     int gen_adaptive = 0, gen_kmax = 1;  // adaptive-K settings from sdv_gen_init
+    bf16 *swa_backup = nullptr;          // sliding-window layers' evicted-slot backups
+    size_t swa_layer_elems = 0;
+    unsigned long long swa_mask = 0;     // bit l: layer l is a sliding-window layer
     int ng_min = 2;                      // n-gram lookup: shortest match length and its pmin scaling
     float ng_pmin = 0.f;
     // phase timing
@@ -149,6 +152,15 @@ enum { P_QKV = 0, P_O = 1, P_GU = 2, P_DOWN = 3, P_LM = 4 };
 // uses region 5 n_layers.
 constexpr int kTraceRegionCtas = 2048;
 constexpr size_t kTraceRegionWords = static_cast<size_t>(kTraceRegionCtas) * 16;
+
+// Sliding-window layers as a bit mask over layers (bit l set: layer l is local).
+unsigned long long local_mask(const sdv_model_cfg &m) {
+    unsigned long long mask = 0;
+    if (m.swa_window <= 0) return 0;
+    for (int l = 0; l < m.n_layers && l < 64; ++l)
+        if (m.swa_global_every <= 0 || (l + 1) % m.swa_global_every != 0) mask |= 1ull << l;
+    return mask;
+}
 
 // n-gram orders indexed per sequence: 1 .. ngram_max_order (0 selects 2).
 int ngram_orders(const sdv_cache_cfg &c) { return c.ngram_max_order > 0 ? c.ngram_max_order : 2; }
@@ -207,6 +219,8 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     s.generated = reinterpret_cast<int *>(take(sizeof(int) * B));
     s.budget = reinterpret_cast<int *>(take(sizeof(int) * B));
     s.kcur = reinterpret_cast<int *>(take(sizeof(int) * B));
+    s.swa_keep = reinterpret_cast<int *>(take(sizeof(int) * B));
+    s.swa_window = m.swa_window > 0 ? m.swa_window : 0;
     s.max_batch = B;
     s.pages_per_seq = pps;
     s.page_size = c.page_size;
@@ -231,6 +245,10 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
         part[i] = reinterpret_cast<float *>(take(sizeof(float) * n));
         cnt[i] = reinterpret_cast<int *>(take(sizeof(int) * plans[i].tiles));
     }
+    // sliding-window backups: per local layer [max_batch][max_span][K|V][nkv][D]
+    const int n_local = __builtin_popcountll(local_mask(m));
+    const size_t swa_layer = static_cast<size_t>(B) * c.max_span * 2 * kvdim;
+    bf16 *swa_backup = reinterpret_cast<bf16 *>(take(sizeof(bf16) * swa_layer * n_local));
     int *done_lm = reinterpret_cast<int *>(take(sizeof(int)));
     auto *keys = reinterpret_cast<unsigned long long *>(take(sizeof(unsigned long long) * kRowsCap));
     float2 *rope = reinterpret_cast<float2 *>(take(sizeof(float2) * static_cast<size_t>(c.max_context) * (D / 2)));
@@ -261,6 +279,9 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
             ctx->plan[i] = plans[i];
         }
         ctx->done_lm = done_lm;
+        ctx->swa_backup = swa_backup;
+        ctx->swa_layer_elems = swa_layer;
+        ctx->swa_mask = local_mask(m);
         ctx->keys = keys;
         ctx->rope = rope;
         ctx->attn_po = apo;
@@ -293,6 +314,11 @@ int check_cfg(const sdv_model_cfg *m, const sdv_cache_cfg *c) {
         return SDV_ERR_ARG;
     if (c->max_context <= 0 || c->ngram_capacity < 0) return SDV_ERR_ARG;
     if (c->ngram_max_order < 0 || c->ngram_max_order > kNgramMaxOrder) return SDV_ERR_ARG;
+    if (m->swa_window < 0 || m->swa_global_every < 0) return SDV_ERR_ARG;
+    if (m->swa_window > 0) {  // a ring of whole pages, never shorter than a span
+        if (m->swa_window % c->page_size || m->swa_window < c->max_span) return SDV_ERR_ARG;
+        if (m->n_layers > 64) return SDV_ERR_UNSUPPORTED;
+    }
     // n-gram contexts pack 21 bits per token
     if (c->ngram_capacity > 0 && m->vocab > (1 << kNgramTokenBits)) return SDV_ERR_UNSUPPORTED;
     return SDV_OK;
@@ -503,6 +529,12 @@ GemmArgs base_args(const sdv_ctx *ctx, int kind, int pidx, int layer) {
     return a;
 }
 
+// The backup of local layer l (its index among the local layers).
+bf16 *swa_backup_of(const sdv_ctx *ctx, int l) {
+    const int li = __builtin_popcountll(ctx->swa_mask & ((1ull << l) - 1ull));
+    return ctx->swa_backup + ctx->swa_layer_elems * li;
+}
+
 // Paged attention of `layer` over the rows prepared in the device state.
 int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *out, size_t out_plane, int B,
                   int max_span, cudaStream_t st) {
@@ -531,6 +563,11 @@ int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *
     a.status = ctx->st.status;
     a.splits = ctx->attn_splits;
     a.layer = layer;
+    if ((ctx->swa_mask >> layer) & 1ull) {
+        a.window = m.swa_window;
+        a.max_span = ctx->c.max_span;
+        a.swa_backup = swa_backup_of(ctx, layer);
+    }
     // the timeline buffer of sdv_fwd_trace, when set (the TMA-fed kernel writes it)
     a.trace = trace_region(ctx, 5 * layer, static_cast<size_t>(ctx->work_cap) * ctx->attn_splits * m.n_kv_heads);
     a.p_lo = ctx->attn_lo;
@@ -629,6 +666,12 @@ GemmArgs qkv_args(const sdv_ctx *ctx, int l) {
     a.q_gain = static_cast<const bf16 *>(ctx->layers[l].q_norm);
     a.k_gain = static_cast<const bf16 *>(ctx->layers[l].k_norm);
     a.kv_layer = ctx->pool + ctx->layer_stride * l;
+    if ((ctx->swa_mask >> l) & 1ull) {  // sliding-window layer: ring slots, keep what a span evicts
+        a.swa_window = m.swa_window;
+        a.max_span = ctx->c.max_span;
+        a.swa_backup = swa_backup_of(ctx, l);
+        a.seq_base = ctx->st.seq_base;
+    }
     return a;
 }
 
@@ -720,6 +763,10 @@ int sdv_create(const sdv_model_cfg *m, const sdv_cache_cfg *c, const sdv_weights
     ctx->attn_tma = c->page_size >= 8 && c->page_size <= kAttnChunk && (c->page_size & (c->page_size - 1)) == 0 &&
                     m->n_kv_heads <= kMaxKvHeads;
     if (ctx->attn_tma) ok &= encode_pool(&ctx->tm_kv, d_kv_pool, *m, *c);
+    if (m->swa_window > 0 && !ctx->attn_tma) {  // sliding-window layers run on the TMA-fed attention only
+        delete ctx;
+        return SDV_ERR_UNSUPPORTED;
+    }
     for (int i = 0; i < 4 && ok; ++i) {
         ok &= encode_planes(&ctx->tm_xb[i], ctx->xb, kRowsCap, H, kNs[i]);
         ok &= encode_planes(&ctx->tm_ao[i], ctx->attn_o, kRowsCap, qdim, kNs[i]);
@@ -919,8 +966,13 @@ int sdv_accept_greedy(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_ro
 
 int sdv_rewind_cache(sdv_ctx *ctx, const int32_t *d_length, int B, void *stream) {
     if (!ctx || !d_length || B <= 0 || B > ctx->c.max_batch) return SDV_ERR_ARG;
-    return rc(launch(ctx, rewind_kernel, dim3(1), dim3(256), 0, static_cast<cudaStream_t>(stream), ctx->st, d_length,
-                     B));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch(ctx, rewind_kernel, dim3(1), dim3(256), 0, st, ctx->st, d_length, B);
+    if (e == cudaSuccess && ctx->swa_mask)
+        e = launch(ctx, swa_restore_kernel, dim3(B, ctx->m.n_layers), dim3(256), 0, st, ctx->st, ctx->pool,
+                   ctx->layer_stride, ctx->swa_mask, static_cast<const bf16 *>(ctx->swa_backup), ctx->swa_layer_elems,
+                   ctx->m.n_kv_heads, ctx->m.head_dim, B);
+    return rc(e);
 }
 
 int sdv_cache_seq_len(sdv_ctx *ctx, int32_t *d_len, void *stream) {

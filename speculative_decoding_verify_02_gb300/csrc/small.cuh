@@ -29,6 +29,8 @@ struct DevState {
     ulonglong2 *ng_keys;  // [max_batch][ng_orders][ng_slots]: n-token context, order n = 1..ng_orders
     int *ng_vals;         // [max_batch][ng_orders][ng_slots]: position of its most recent follower
     int *cur_tok, *generated, *budget, *kcur;  // [max_batch]
+    int *swa_keep;      // [max_batch] rows of the last forward's span kept by the last rewind (sliding window)
+    int swa_window;     // > 0: the model has sliding-window layers
     int max_batch, pages_per_seq, page_size, n_pages_total, max_rows, max_span, work_cap;
     int ngram_cap, ng_slots, ng_orders;
 };
@@ -280,6 +282,11 @@ __global__ void rewind_kernel(DevState s, const int *length, int B) {
                 ok = 0;
                 continue;
             }
+            // sliding-window rings keep only what the last forward evicted
+            if (s.swa_window > 0 && len < s.seq_base[b] && s.seq_len[b] > s.swa_window) {
+                ok = 0;
+                continue;
+            }
             const int keep = (len + s.page_size - 1) / s.page_size;
             rel_s[b] = max(0, s.n_pages[b] - keep);
         }
@@ -306,6 +313,39 @@ __global__ void rewind_kernel(DevState s, const int *length, int B) {
         }
         s.n_pages[b] = n - rel_s[b];
         s.seq_len[b] = len;
+    }
+    // rows of the last forward kept (the rest are restored in the sliding-window rings)
+    if (s.swa_window > 0)
+        for (int b = threadIdx.x; b < B; b += blockDim.x) {
+            const int len = length[b];
+            s.swa_keep[b] = len < 0 ? 1 << 30 : len - s.seq_base[b];
+        }
+}
+
+// [TS] sliding-window caches and rollback: for every local layer and sequence, the slots of the
+// last forward's rejected rows (span rows at or past the kept count) get back the positions they
+// held, from the layer's backup; a full acceptance restores nothing. Grid (B, n_layers).
+__global__ void swa_restore_kernel(DevState s, bf16 *pool, size_t layer_stride, const unsigned long long local_mask,
+                                   const bf16 *backup, size_t backup_layer_stride, int nkv, int D, int B) {
+    pdl_trigger();
+    pdl_wait();
+    const int b = blockIdx.x, l = blockIdx.y;
+    if (b >= B || !((local_mask >> l) & 1ull)) return;
+    const int li = __popcll(local_mask & ((1ull << l) - 1ull));  // index among the local layers
+    const int p = s.seq_base[b], S = s.row_off[b + 1] - s.row_off[b], keep = max(0, s.swa_keep[b]);
+    const int W = s.swa_window, P = s.page_size;
+    const int row = D * nkv;  // elements of one K (or V) row of all heads
+    for (int j = keep; j < S && j < s.max_span; ++j) {
+        const int u = p + j - W;  // the position span row j evicted
+        if (u < 0) continue;
+        const int page = s.page_table[static_cast<size_t>(b) * s.pages_per_seq + ((p + j) % W) / P];
+        if (page < 0 || page >= s.n_pages_total) continue;
+        const bf16 *src = backup + li * backup_layer_stride + (static_cast<size_t>(b) * s.max_span + j) * 2 * row;
+        bf16 *dst = pool + l * layer_stride;
+        for (int e = threadIdx.x; e < 2 * row; e += blockDim.x) {
+            const int kv = e / row, h = (e % row) / D, d = e % D;
+            dst[(((static_cast<size_t>(page) * 2 + kv) * nkv + h) * P + (p + j) % P) * D + d] = src[e];
+        }
     }
 }
 

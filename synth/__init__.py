@@ -116,10 +116,24 @@ class Shape:
     rms_eps: float = 1e-6
     rope_theta: float = 1e6
     qk_norm: bool = True
+    swa_window: int = 0        # > 0: local (sliding-window) layers attend the last swa_window positions
+    swa_global_every: int = 0  # with a window: layer l is global iff (l + 1) % swa_global_every == 0 (0: none)
 
     def with_layers(self, n: int) -> "Shape":
         return Shape(f"{self.name}-L{n}", n, self.hidden, self.n_q_heads, self.n_kv_heads, self.head_dim,
-                     self.ffn, self.vocab, self.rms_eps, self.rope_theta, self.qk_norm)
+                     self.ffn, self.vocab, self.rms_eps, self.rope_theta, self.qk_norm, self.swa_window,
+                     self.swa_global_every)
+
+    def with_window(self, window: int, global_every: int = 0) -> "Shape":
+        return Shape(f"{self.name}-W{window}", self.n_layers, self.hidden, self.n_q_heads, self.n_kv_heads,
+                     self.head_dim, self.ffn, self.vocab, self.rms_eps, self.rope_theta, self.qk_norm, window,
+                     global_every)
+
+    def is_local(self, layer: int) -> bool:
+        """Whether `layer` is a sliding-window layer."""
+        if self.swa_window <= 0:
+            return False
+        return self.swa_global_every <= 0 or (layer + 1) % self.swa_global_every != 0
 
     def tensor_shapes(self) -> dict:
         H, D, F, V = self.hidden, self.head_dim, self.ffn, self.vocab

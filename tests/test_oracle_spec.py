@@ -261,3 +261,67 @@ def test_multi_order_index_matches_brute_force(vocab):
                     ctx = h[L + 1 - n_req:L + 1]
                     assert any(h[j - n_req:j] == ctx and h[j:j + len(brute)] == brute
                                for j in range(n_req, L + 1))
+
+
+# ----------------------------------------------------------------------------- sliding-window ring
+
+def _ring_trace(rule, W, seed, steps=400, max_span=None):
+    from oracle.ring import WindowRing
+    rng = np.random.default_rng(seed)
+    ring = WindowRing(W, rule)
+    ok = True
+    for _ in range(steps):
+        S = int(rng.integers(1, (max_span or W) + 1))
+        seen = ring.verify(S)
+        ok &= all(seen)
+        m = int(rng.integers(0, S)) if rng.random() < 0.7 else S - 1      # partial or full acceptance
+        ring.accept(m)
+        ok &= ring.window_intact()
+    return ok
+
+
+@pytest.mark.parametrize("W,max_span", [(8, 8), (16, 5), (32, 17)])
+def test_window_ring_rule_keeps_every_window(W, max_span):
+    """[TS] sliding-window caches and rollback: saving what a verify evicts and putting back the
+    rejected rows (nothing on a full acceptance) keeps every row's window and the next token's
+    window in the one-window ring, over random spans and acceptances well past the wrap."""
+    for seed in range(10):
+        assert _ring_trace("rejected", W, seed, max_span=max_span)
+
+
+def test_window_ring_wrong_rules_fail():
+    """The two rules the page rules out: never restoring loses evicted positions once two or more
+    rows are rejected; restoring on a full acceptance puts evicted positions over committed rows."""
+    assert not all(_ring_trace("never", 16, s) for s in range(5))
+    assert not all(_ring_trace("always", 16, s) for s in range(5))
+    from oracle.ring import WindowRing
+    r = WindowRing(8, "never")                 # the page's example: two rows rejected past the wrap
+    r.verify(8); r.accept(7)
+    r.verify(5); r.accept(1)                   # rows 2..4 rejected; the next token needs position 3+...
+    assert not r.window_intact()
+    r = WindowRing(8, "rejected")
+    r.verify(8); r.accept(7)
+    r.verify(5); r.accept(1)
+    assert r.window_intact()
+
+
+def test_window_attention_pins():
+    """The oracle's sliding-window attention: a window as long as the context is full causal
+    attention; a window of one returns the row's own value; otherwise it equals full attention over
+    the window's keys alone."""
+    from oracle import attention_rows
+    rng = np.random.default_rng(9)
+    T, S, nq, nkv, D = 40, 6, 4, 2, 16
+    q = rng.standard_normal((S, nq, D))
+    K, V = rng.standard_normal((T, nkv, D)), rng.standard_normal((T, nkv, D))
+    pos = np.arange(T - S, T)
+    full = attention_rows(q, K, V, pos, 0.25)
+    np.testing.assert_array_equal(attention_rows(q, K, V, pos, 0.25, window=T), full)
+    one = attention_rows(q, K, V, pos, 0.25, window=1)
+    np.testing.assert_allclose(one, np.repeat(V[pos], nq // nkv, axis=1), rtol=0, atol=1e-15)
+    W = 9
+    win = attention_rows(q, K, V, pos, 0.25, window=W)
+    for i, t in enumerate(pos):
+        lo = t - W + 1
+        ref = attention_rows(q[i:i + 1], K[lo:t + 1], V[lo:t + 1], np.array([W - 1]), 0.25)
+        np.testing.assert_allclose(win[i], ref[0], rtol=1e-13, atol=1e-13)
