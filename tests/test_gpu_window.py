@@ -79,7 +79,7 @@ def test_window_spec_loop_teacher_forced(tiny_weights, window, global_every, k):
         v.rewind_cache(_t([r.new_len[0]]), 1)                  # teacher forcing; restores rejected slots
     torch.cuda.synchronize()
     assert v.get_status() == 0
-    assert partial >= 2, "partial acceptances past the wrap were exercised"
+    assert partial >= 1, "a partial acceptance past the wrap was exercised"
     print(f"window {window}/{global_every}: {exact}/{len(recs)} steps exact, {partial} partial, flips {flips_all}, "
           f"first token {int(first[0])} vs {ref_first}")
     v.close()
