@@ -27,6 +27,10 @@ struct GemmArgs {
     int kind;
     int tiles, splits, kps, k_blocks;  // output tiles, K splits, k-blocks per split, total k-blocks (64 wide)
     int l2_ahead;                      // k-blocks prefetched into L2 beyond the shared-memory stages
+    // the next projection's weights pulled into L2 before this launch's inputs are ready (while the
+    // previous kernel, the attention, leaves HBM idle): its first next_kblocks k-blocks of every one
+    // of its next_tiles gate/up tiles (maps tmA1, tmA2; 64 rows each), spread over this grid's CTAs
+    int next_tiles, next_kblocks;
     int n_out;                         // valid output features (ffn for SwiGLU)
     int rows_cap;                      // rows of the activation / ss buffers (plane stride in rows)
     const int *nrows;                  // device: rows present (R)
@@ -458,6 +462,19 @@ __device__ __forceinline__ void prefetch_a(const CUtensorMap *tmA0, const CUtens
 }
 
 
+// The first k-blocks of the next (gate/up) projection into L2, k-block-major, spread over the grid.
+#ifndef SDV_NEXT_PREFETCH_AT
+#define SDV_NEXT_PREFETCH_AT 1  // 0: before this launch's inputs are ready; 1: after its own loads
+#endif
+__device__ __forceinline__ void prefetch_next(const CUtensorMap *tmG, const CUtensorMap *tmU, const GemmArgs &a) {
+    const int units = a.next_tiles * a.next_kblocks;
+    for (int u = static_cast<int>(blockIdx.x); u < units; u += static_cast<int>(gridDim.x)) {
+        const int t = u % a.next_tiles, kc = (u / a.next_tiles) * 64;
+        tma_prefetch_2d(tmG, kc, t * 64);
+        tma_prefetch_2d(tmU, kc, t * 64);
+    }
+}
+
 template <int N, int KIND>
 __global__ void __launch_bounds__(kGemmThreads, 2)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -519,6 +536,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             // optionally pull further weight tiles into L2 while the previous kernel runs
             const int ahead = min(nk, pre + a.l2_ahead);
             for (int i = pre; i < ahead; ++i) prefetch_a<KIND>(&tmA0, &tmA1, &tmA2, a, tile, (kb0 + i) * 64);
+#if SDV_NEXT_PREFETCH_AT == 0
+            if constexpr (KIND == EPI_RESID) prefetch_next(&tmA1, &tmA2, a);
+#endif
             pdl_wait();  // activations come from the previous kernel
             gemm_stamp(a, 1);
             for (int i = 0; i < pre; ++i)
@@ -540,6 +560,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 tma_load_3d(sa + S::A_BYTES, &tmB, &full_bar[s], kc, 0, 0);
                 issued = i + 1;
             }
+#if SDV_NEXT_PREFETCH_AT == 1
+            if constexpr (KIND == EPI_RESID) prefetch_next(&tmA1, &tmA2, a);
+#endif
             if (timed_out) {
                 // error path: the copies already issued must land before this CTA may leave (its
                 // shared memory goes to the next CTA); each stage's last issued phase, bounded
@@ -621,13 +644,15 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         tc_fence_after();
         if (threadIdx.x == 0) gemm_stamp(a, 4);
         const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const int f = threadIdx.x;
+        // park the partial as [row][lane][4]: feature 32 i + l at l * 4 + i, so that the lane that
+        // finishes features l, l+32, l+64, l+96 of a row reads them as one 16-byte vector
+        const int f = threadIdx.x, fpos = (f & 31) * 4 + (f >> 5);
         float v[32];
         for (int c0 = 0; c0 < R; c0 += 32) {
             acc_load(taddr, c0, N, v);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                if (c0 + j < R) red[(c0 + j) * 128 + f] = v[j];
+                if (c0 + j < R) red[(c0 + j) * 128 + fpos] = v[j];
         }
     }
     // every partial of the tile is parked in shared memory (of each CTA of the cluster)
@@ -648,18 +673,27 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 for (int i = 0; i < 4; ++i) x[u][i] = 0.f;
                 if (r < s1) {
                     if (clustered) {
+                        // every split's 16 bytes in flight together, then summed in split order
+                        float4 xs[kMaxSplits];
+#pragma unroll
+                        for (int q = 0; q < kMaxSplits; ++q)
+                            if (q < a.splits)
+                                xs[q] = ld_dsmem_f4(mapa_shared(red_local, static_cast<uint32_t>(q)) + r * 512 + lane * 16);
 #pragma unroll
                         for (int q = 0; q < kMaxSplits; ++q) {  // fixed split order
                             if (q < a.splits) {
-                                const uint32_t base =
-                                    mapa_shared(red_local, static_cast<uint32_t>(q)) + r * 512 + lane * 4;
-#pragma unroll
-                                for (int i = 0; i < 4; ++i) x[u][i] += ld_dsmem(base + 128 * i);
+                                x[u][0] += xs[q].x;
+                                x[u][1] += xs[q].y;
+                                x[u][2] += xs[q].z;
+                                x[u][3] += xs[q].w;
                             }
                         }
                     } else {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) x[u][i] = red[r * 128 + lane + 32 * i];
+                        const float4 xv = *reinterpret_cast<const float4 *>(&red[r * 128 + lane * 4]);
+                        x[u][0] = xv.x;
+                        x[u][1] = xv.y;
+                        x[u][2] = xv.z;
+                        x[u][3] = xv.w;
                     }
                 }
             }
@@ -686,7 +720,9 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
         }
     }
     if (threadIdx.x == 0) gemm_stamp(a, 7);
-    if (clustered) cluster_sync();  // no CTA leaves while its partial may still be read
+    // this CTA's reads of the others' partials are done; it leaves only once every CTA of the
+    // cluster has arrived (no CTA leaves while its partial may still be read)
+    if (clustered) cluster_arrive();
     if constexpr (KIND == EPI_LMHEAD) {
         if (warp < 4) {
             __threadfence();
@@ -707,11 +743,12 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
     }
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) gemm_stamp(a, 8);
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, S::TMEM_COLS);
     }
+    if (clustered) cluster_wait();
+    if (threadIdx.x == 0) gemm_stamp(a, 8);
 }
 
 }  // namespace sdv

@@ -28,6 +28,11 @@ struct GemmPlan {
 };
 
 constexpr int kRowsCap = 128;     // activation rows held in the workspace (max_rows <= 128)
+// k-blocks (64 columns) of every gate/up tile that the O projection pulls into L2 ahead of time
+#ifndef SDV_NEXT_PREFETCH_KBLOCKS
+#define SDV_NEXT_PREFETCH_KBLOCKS 0
+#endif
+constexpr int kNextPrefetchKBlocks = SDV_NEXT_PREFETCH_KBLOCKS;
 constexpr int kNs[4] = {16, 32, 64, 128};
 
 int n_index(int max_rows) {
@@ -870,6 +875,10 @@ int spec_forward_impl(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_ro
         // (21 MB) are pulled into L2 during the attention, when HBM is otherwise idle.
         a = base_args(ctx, EPI_RESID, P_O, l);
         a.l2_ahead = 64;
+        // the O projection runs beside the attention, when HBM is otherwise idle: it also pulls the
+        // first k-blocks of the gate/up weights into L2
+        a.next_tiles = ctx->plan[P_GU].tiles;
+        a.next_kblocks = std::min(ctx->plan[P_GU].k_blocks, kNextPrefetchKBlocks);
         a.n_out = m.hidden;
         a.x = ctx->x;
         a.xb = ctx->xb;
@@ -877,7 +886,7 @@ int spec_forward_impl(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_ro
         a.ss_out = ctx->ss;
         {
             PhaseMark pm(ctx, 3, st);
-            e = launch_gemm(ctx, ni, ctx->tm_wo[l], ctx->tm_wo[l], ctx->tm_wo[l], ctx->tm_ao[ni], a,
+            e = launch_gemm(ctx, ni, ctx->tm_wo[l], ctx->tm_wg[l], ctx->tm_wu[l], ctx->tm_ao[ni], a,
                             ctx->plan[P_O].tiles * ctx->plan[P_O].splits, st);
         }
         if (e != cudaSuccess) return SDV_ERR_CUDA;
