@@ -176,7 +176,9 @@ def trace_launches(buf, n_layers):
         launches.append({"name": name, "start": int(c[:, 0].min()), "ready": int(ready.min()),
                          "end": int(c[:, end_ev].max()),
                          "first_stage": None if attn else int(c[:, 2].max()),
-                         "last_mma": None if attn else int(c[:, 3].max())})
+                         "last_mma": None if attn else int(c[:, 3].max()),
+                         "reduced": None if attn else int(c[:, 6].max()),
+                         "rows": None if attn else int(c[:, 7].max())})
     prev_end = launches[0]["start"]
     for x in launches:
         x["excl"] = x["end"] - prev_end
@@ -195,7 +197,11 @@ def trace_launches(buf, n_layers):
             "excl_us": {**{n: med(n, "excl") for n in names}, "lm_head": med("lm_head", "excl")},
             "handoff_us": {n: med(n, "handoff") for n in names},
             "stream_us": {n: round(statistics.median(x["last_mma"] - x["first_stage"] for x in launches
-                                                     if x["name"] == n) / 1e3, 2) for n in PROJ}}
+                                                     if x["name"] == n) / 1e3, 2) for n in PROJ},
+            "tail_us": {n: {k: round(statistics.median(x[b] - x[a] for x in launches if x["name"] == n) / 1e3, 2)
+                            for k, a, b in (("first_stage", "ready", "first_stage"), ("park_sync", "last_mma", "reduced"),
+                                            ("rows", "reduced", "rows"), ("exit", "rows", "end"))}
+                        for n in PROJ}}
 
 
 # ----------------------------------------------------------------------------- the headline (b1)
@@ -383,11 +389,14 @@ def run_ours(args, rank, world, dev):
         "in_graph": {"exclusive_us_per_layer": tr["excl_us"],
                      "handoff_us": tr["handoff_us"],
                      "gemm_stream_us": tr["stream_us"],
+                     "gemm_phases_us": tr["tail_us"],
                      "attention_ms_per_step": round(tr["attention_ns"] / 1e6, 4),
                      "traced_step_ms": round(tr["step_ns"] / 1e6, 4),
                      "note": ("exclusive window = a launch's end minus the previous launch's end; handoff "
                               "= first CTA past its wait minus the previous launch's end; stream = first "
-                              "stage landed to last MMA issued (median over layers)")},
+                              "stage landed to last MMA issued; phases: first stage after the wait, partial "
+                              "parked + cluster barrier after the last MMA, row epilogue, exit (medians "
+                              "over layers, latest CTA of each)")},
         "phases_ms_per_step_serialised": {p: round(prof[p][0] / args.steps, 4) for p in prof},
         "e2e": {"value": round(e2e_committed_all / e2e_max, 3), "unit": "tok/s",
                 "h2d_bytes_per_step": K_DRAFT * 4, "d2h_bytes_per_step": (K_DRAFT + 2) * 4},
