@@ -51,7 +51,8 @@ EMBED_BYTES_PER_ROW = 2560 * 2
 # 2-layer case of the same shapes (profiles/gemm_tcgen05_qwen3_4b_verify_N16.md); a launch streams
 # its own weights, so a 36-layer step is 36 layers of the first four plus one LM head.
 GEMM_TRAFFIC_MB = {"qkv": 31.6998, "o": 21.3698, "gate_up": 99.9877, "down": 50.5655, "lm_head": 778.2215}
-TRACE_REGION_WORDS = 2048 * 16            # sdv_fwd_trace: 16 stamps x 2048 CTAs per launch
+from speculative_decoding_verify_02_gb300 import TRACE_REGION_CTAS, TRACE_STAMPS  # noqa: E402
+TRACE_REGION_WORDS = TRACE_REGION_CTAS * TRACE_STAMPS  # sdv_fwd_trace: one region per launch
 PROJ = ("qkv", "o", "gate_up", "down")
 
 
@@ -157,7 +158,7 @@ def trace_launches(buf, n_layers):
     first CTA past its wait on the previous kernel ("ready"), and its last CTA end (ns). Each
     launch's exclusive window is its end minus the previous launch's end: the windows partition
     the step, so PDL's early CTA starts are not counted twice."""
-    t = buf.view(-1, 2048, 16).cpu().numpy()
+    t = buf.view(-1, TRACE_REGION_WORDS // 16, 16).cpu().numpy()
     first = t[1, :, 0]
     t0 = int(first[first > 0].min())          # every CTA of layer 0's QKV launch runs each step
     order = []
@@ -479,6 +480,17 @@ def run_verify_workload(args, name, contexts, seed, dev, steps=None, warmup=None
     clk = clocks.stop()
     committed = total_len() - L0
     assert v.get_status() == 0
+    # the device timeline of a few more steps (graph recaptured with the trace on; the last one read)
+    trace_buf = torch.zeros((5 * shape.n_layers + 1) * TRACE_REGION_WORDS, dtype=torch.int64, device="cuda")
+    v.fwd_trace(trace_buf)
+    loop.capture(**kw)
+    v.fwd_trace(None)
+    for _ in range(3):
+        loop.replay()
+    timed_replays(loop, 3, s)
+    tr = trace_launches(trace_buf, shape.n_layers)
+    assert v.get_status() == 0
+    del trace_buf
     v.profile_enable(True)  # per-phase device time (events around each launch group, eager steps)
     v.profile_read()
     n_prof = min(steps, 5)
@@ -504,6 +516,11 @@ def run_verify_workload(args, name, contexts, seed, dev, steps=None, warmup=None
         "step_roofline_frac": round(step_bytes / (step_ms * 1e-3) / 1e9 / peak, 4),
         "step_bytes": int(step_bytes), "peak_kind": peak_kind, "clocks": clk, "setup_s": round(setup_s, 1),
         "phases_ms_per_step_serialised": {p: round(prof[p][0] / n_prof, 4) for p in prof},
+        "in_graph": {"exclusive_us_per_layer": tr["excl_us"], "handoff_us": tr["handoff_us"],
+                     "gemm_stream_us": tr["stream_us"], "gemm_phases_us": tr["tail_us"],
+                     "attention_ms_per_step": round(tr["attention_ns"] / 1e6, 4),
+                     "gemm_ms_per_step": round(tr["gemm_ns"] / 1e6, 4),
+                     "traced_step_ms": round(tr["step_ns"] / 1e6, 4)},
     }
 
 
@@ -743,6 +760,7 @@ def main():
                                           "verify_hbm_gbs", "step_roofline_frac", "step_bytes", "clocks")}
             out[key]["config"] = r["config"]
             out[key]["phases_ms_per_step_serialised"] = r["phases_ms_per_step_serialised"]
+            out[key]["in_graph"] = r["in_graph"]
             torch.cuda.empty_cache()
     if rank == 0:
         if args.cpu_baseline and world == 1:

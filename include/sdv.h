@@ -293,11 +293,11 @@ int sdv_profile_read(sdv_ctx *ctx, float *h_ms, int32_t *h_count);
  * changing its launches. With d_buf non-null, later sdv_spec_forward calls
  * write %globaltimer stamps (nanoseconds) into it; entries of events that did
  * not happen keep their old value. The buffer is cut into regions of
- * 2048 CTAs x 16 stamps (262,144 bytes), one per launch of a forward:
+ * 8192 CTAs x 16 stamps (1,048,576 bytes), one per launch of a forward:
  * layer l uses region 5l for its attention and 5l + 1 + p for its GEMM
  * launches (p = 0 QKV, 1 O, 2 gate/up, 3 down); the LM head uses region
- * 5 n_layers. CTA c of a launch writes d_buf[region * 32768 + c * 16 + e]; a
- * launch with more than 2048 CTAs, or whose region lies past the buffer, is
+ * 5 n_layers. CTA c of a launch writes d_buf[region * 131072 + c * 16 + e]; a
+ * launch with more than 8192 CTAs, or whose region lies past the buffer, is
  * not traced.
  *   GEMM launches: e = 0 CTA start, 1 activations ready (after the wait on
  *   the previous kernel), 2 first stage landed, 3 last MMA issued,

@@ -36,7 +36,7 @@ EXPORTS = (
 )
 PHASES = ("prepare", "qkv_gemm", "attention", "o_gemm", "gateup_gemm", "down_gemm", "lmhead_gemm")
 # sdv_fwd_trace: stamps per CTA, CTAs per region (one region per launch of a forward)
-TRACE_STAMPS, TRACE_REGION_CTAS = 16, 2048
+TRACE_STAMPS, TRACE_REGION_CTAS = 16, 8192
 
 
 class SdvError(RuntimeError):

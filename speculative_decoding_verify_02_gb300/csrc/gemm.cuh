@@ -27,10 +27,6 @@ struct GemmArgs {
     int kind;
     int tiles, splits, kps, k_blocks;  // output tiles, K splits, k-blocks per split, total k-blocks (64 wide)
     int l2_ahead;                      // k-blocks prefetched into L2 beyond the shared-memory stages
-    // the next projection's weights pulled into L2 before this launch's inputs are ready (while the
-    // previous kernel, the attention, leaves HBM idle): its first next_kblocks k-blocks of every one
-    // of its next_tiles gate/up tiles (maps tmA1, tmA2; 64 rows each), spread over this grid's CTAs
-    int next_tiles, next_kblocks;
     int n_out;                         // valid output features (ffn for SwiGLU)
     int rows_cap;                      // rows of the activation / ss buffers (plane stride in rows)
     const int *nrows;                  // device: rows present (R)
@@ -462,19 +458,6 @@ __device__ __forceinline__ void prefetch_a(const CUtensorMap *tmA0, const CUtens
 }
 
 
-// The first k-blocks of the next (gate/up) projection into L2, k-block-major, spread over the grid.
-#ifndef SDV_NEXT_PREFETCH_AT
-#define SDV_NEXT_PREFETCH_AT 1  // 0: before this launch's inputs are ready; 1: after its own loads
-#endif
-__device__ __forceinline__ void prefetch_next(const CUtensorMap *tmG, const CUtensorMap *tmU, const GemmArgs &a) {
-    const int units = a.next_tiles * a.next_kblocks;
-    for (int u = static_cast<int>(blockIdx.x); u < units; u += static_cast<int>(gridDim.x)) {
-        const int t = u % a.next_tiles, kc = (u / a.next_tiles) * 64;
-        tma_prefetch_2d(tmG, kc, t * 64);
-        tma_prefetch_2d(tmU, kc, t * 64);
-    }
-}
-
 template <int N, int KIND>
 __global__ void __launch_bounds__(kGemmThreads, 2)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -536,9 +519,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
             // optionally pull further weight tiles into L2 while the previous kernel runs
             const int ahead = min(nk, pre + a.l2_ahead);
             for (int i = pre; i < ahead; ++i) prefetch_a<KIND>(&tmA0, &tmA1, &tmA2, a, tile, (kb0 + i) * 64);
-#if SDV_NEXT_PREFETCH_AT == 0
-            if constexpr (KIND == EPI_RESID) prefetch_next(&tmA1, &tmA2, a);
-#endif
             pdl_wait();  // activations come from the previous kernel
             gemm_stamp(a, 1);
             for (int i = 0; i < pre; ++i)
@@ -560,9 +540,6 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                 tma_load_3d(sa + S::A_BYTES, &tmB, &full_bar[s], kc, 0, 0);
                 issued = i + 1;
             }
-#if SDV_NEXT_PREFETCH_AT == 1
-            if constexpr (KIND == EPI_RESID) prefetch_next(&tmA1, &tmA2, a);
-#endif
             if (timed_out) {
                 // error path: the copies already issued must land before this CTA may leave (its
                 // shared memory goes to the next CTA); each stage's last issued phase, bounded

@@ -28,11 +28,6 @@ struct GemmPlan {
 };
 
 constexpr int kRowsCap = 128;     // activation rows held in the workspace (max_rows <= 128)
-// k-blocks (64 columns) of every gate/up tile that the O projection pulls into L2 ahead of time
-#ifndef SDV_NEXT_PREFETCH_KBLOCKS
-#define SDV_NEXT_PREFETCH_KBLOCKS 0
-#endif
-constexpr int kNextPrefetchKBlocks = SDV_NEXT_PREFETCH_KBLOCKS;
 constexpr int kNs[4] = {16, 32, 64, 128};
 
 int n_index(int max_rows) {
@@ -155,7 +150,7 @@ enum { P_QKV = 0, P_O = 1, P_GU = 2, P_DOWN = 3, P_LM = 4 };
 // Timeline buffer (sdv_fwd_trace): one region of kTraceRegionCtas x 16 stamps per launch of a
 // step. Layer l uses regions 5l (attention) and 5l + 1 + p (GEMM of plan p, p < 4); the LM head
 // uses region 5 n_layers.
-constexpr int kTraceRegionCtas = 2048;
+constexpr int kTraceRegionCtas = 8192;
 constexpr size_t kTraceRegionWords = static_cast<size_t>(kTraceRegionCtas) * 16;
 
 // Sliding-window layers as a bit mask over layers (bit l set: layer l is local).
@@ -875,10 +870,6 @@ int spec_forward_impl(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_ro
         // (21 MB) are pulled into L2 during the attention, when HBM is otherwise idle.
         a = base_args(ctx, EPI_RESID, P_O, l);
         a.l2_ahead = 64;
-        // the O projection runs beside the attention, when HBM is otherwise idle: it also pulls the
-        // first k-blocks of the gate/up weights into L2
-        a.next_tiles = ctx->plan[P_GU].tiles;
-        a.next_kblocks = std::min(ctx->plan[P_GU].k_blocks, kNextPrefetchKBlocks);
         a.n_out = m.hidden;
         a.x = ctx->x;
         a.xb = ctx->xb;
@@ -886,7 +877,7 @@ int spec_forward_impl(sdv_ctx *ctx, const int32_t *d_tokens, const int32_t *d_ro
         a.ss_out = ctx->ss;
         {
             PhaseMark pm(ctx, 3, st);
-            e = launch_gemm(ctx, ni, ctx->tm_wo[l], ctx->tm_wg[l], ctx->tm_wu[l], ctx->tm_ao[ni], a,
+            e = launch_gemm(ctx, ni, ctx->tm_wo[l], ctx->tm_wo[l], ctx->tm_wo[l], ctx->tm_ao[ni], a,
                             ctx->plan[P_O].tiles * ctx->plan[P_O].splits, st);
         }
         if (e != cudaSuccess) return SDV_ERR_CUDA;
