@@ -174,12 +174,17 @@ def trace_launches(buf, n_layers):
         ok = (c[:, 0] >= t0) & (c[:, end_ev] >= c[:, 0])
         c = c[ok]
         ready = c[:, 0] if attn else c[:, 1]      # the attention stamps its start after its wait
+        pass0 = None
+        if not attn:  # the first row pass of the CTAs' first warp: partials summed, rows written
+            w = (c[:, 9] >= c[:, 6]) & (c[:, 10] >= c[:, 9]) & (c[:, 6] > 0)
+            if w.any():
+                pass0 = (float(np.median(c[w, 9] - c[w, 6])), float(np.median(c[w, 10] - c[w, 9])))
         launches.append({"name": name, "start": int(c[:, 0].min()), "ready": int(ready.min()),
                          "end": int(c[:, end_ev].max()),
                          "first_stage": None if attn else int(c[:, 2].max()),
                          "last_mma": None if attn else int(c[:, 3].max()),
                          "reduced": None if attn else int(c[:, 6].max()),
-                         "rows": None if attn else int(c[:, 7].max())})
+                         "rows": None if attn else int(c[:, 7].max()), "pass0": pass0})
     prev_end = launches[0]["start"]
     for x in launches:
         x["excl"] = x["end"] - prev_end
@@ -199,9 +204,14 @@ def trace_launches(buf, n_layers):
             "handoff_us": {n: med(n, "handoff") for n in names},
             "stream_us": {n: round(statistics.median(x["last_mma"] - x["first_stage"] for x in launches
                                                      if x["name"] == n) / 1e3, 2) for n in PROJ},
-            "tail_us": {n: {k: round(statistics.median(x[b] - x[a] for x in launches if x["name"] == n) / 1e3, 2)
-                            for k, a, b in (("first_stage", "ready", "first_stage"), ("park_sync", "last_mma", "reduced"),
-                                            ("rows", "reduced", "rows"), ("exit", "rows", "end"))}
+            "tail_us": {n: {**{k: round(statistics.median(x[b] - x[a] for x in launches if x["name"] == n) / 1e3, 2)
+                               for k, a, b in (("first_stage", "ready", "first_stage"),
+                                               ("park_sync", "last_mma", "reduced"), ("rows", "reduced", "rows"),
+                                               ("exit", "rows", "end"))},
+                            **{k: round(statistics.median(x["pass0"][i] for x in launches
+                                                          if x["name"] == n and x["pass0"]) / 1e3, 2)
+                               for i, k in enumerate(("rows_sum_first_pass", "rows_write_first_pass"))
+                               if any(x["name"] == n and x["pass0"] for x in launches)}}
                         for n in PROJ}}
 
 
@@ -397,7 +407,9 @@ def run_ours(args, rank, world, dev):
                               "= first CTA past its wait minus the previous launch's end; stream = first "
                               "stage landed to last MMA issued; phases: first stage after the wait, partial "
                               "parked + cluster barrier after the last MMA, row epilogue, exit (medians "
-                              "over layers, latest CTA of each)")},
+                              "over layers, latest CTA of each); the row epilogue's first pass of four rows "
+                              "per warp, split into summing the split partials and writing the rows "
+                              "(medians over CTAs and layers)")},
         "phases_ms_per_step_serialised": {p: round(prof[p][0] / args.steps, 4) for p in prof},
         "e2e": {"value": round(e2e_committed_all / e2e_max, 3), "unit": "tok/s",
                 "h2d_bytes_per_step": K_DRAFT * 4, "d2h_bytes_per_step": (K_DRAFT + 2) * 4},

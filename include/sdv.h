@@ -302,7 +302,8 @@ int sdv_profile_read(sdv_ctx *ctx, float *h_ms, int32_t *h_count);
  *   GEMM launches: e = 0 CTA start, 1 activations ready (after the wait on
  *   the previous kernel), 2 first stage landed, 3 last MMA issued,
  *   4 accumulator ready, 5 partial parked, 6 all partials of the tile parked,
- *   7 rows finished, 8 CTA end.
+ *   7 rows finished, 8 CTA end; for the first three passes p of four rows of
+ *   the first warp: 9 + 2p the rows' partials summed, 10 + 2p the rows written.
  *   Attention (CTA in launch order): e = 0 start, 1 Q and page ids in, 2 first
  *   chunk landed, 3 chunks done, 4 the CTA states of its cluster in place,
  *   5 cluster merge done, 6 CTA end, 10 second chunk landed, 11 second chunk

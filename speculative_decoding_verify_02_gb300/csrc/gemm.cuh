@@ -674,6 +674,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                     }
                 }
             }
+            if (threadIdx.x == 0 && p < 3) gemm_stamp(a, 9 + 2 * p);  // the pass's partials in registers
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int r = s0 + warp + 16 * p + 4 * u;
@@ -694,6 +695,7 @@ __global__ void __launch_bounds__(kGemmThreads, 2)
                     }
                 }
             }
+            if (threadIdx.x == 0 && p < 3) gemm_stamp(a, 10 + 2 * p);  // the pass's rows written
         }
     }
     if (threadIdx.x == 0) gemm_stamp(a, 7);

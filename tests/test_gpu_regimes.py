@@ -68,7 +68,14 @@ def test_attention_merge_in_kernel_and_by_merge_kernel(L):
     _attention_batch([L], [8], 16384, f"merge{L}")
 
 
-def _attention_batch(lens, S, max_context, tag):
+@pytest.mark.parametrize("page", [8, 32, 64, 128])
+def test_attention_page_sizes(page):
+    """The K/V copies at other page sizes: one box per page below 64 slots, one per 64-slot half of a
+    128-slot page; ragged contexts so chunks end mid-page and mid-box, one multi-group sequence."""
+    _attention_batch([37, 700, 1500, 2100], [8, 3, 17, 5], 2200, f"page{page}", page=page)
+
+
+def _attention_batch(lens, S, max_context, tag, page=P):
     import torch
     import speculative_decoding_verify_02_gb300 as sdv
     shape = synth.Shape("attn-4b-heads", 1, 256, 32, 8, 128, 256, 256)     # the 4B model's heads
@@ -77,6 +84,7 @@ def _attention_batch(lens, S, max_context, tag):
     spans = tag
     R = sum(S)
     assert R <= 128
+    P = page
     need = sum(-(-(L + s) // P) for L, s in zip(lens, S))
     v = sdv.Verifier(shape, weights, page_size=P, n_pages=need + 8, max_batch=B, max_rows=128, max_span=17,
                      max_context=max_context)
