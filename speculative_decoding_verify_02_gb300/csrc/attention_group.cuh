@@ -83,7 +83,11 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     __shared__ int last_s;
 
     pdl_trigger();
-    pdl_wait();
+    // The forward's prepare kernel finished before this kernel started (it does not trigger its
+    // dependents early), so the work list, the page table and the K/V of every position before the
+    // span (written by earlier steps) are final here: they are read, and the copies of chunks that
+    // hold only such positions issued, before the wait. The span's own K/V and the queries come
+    // from the QKV projection this kernel follows, after the wait.
     // optional timeline: 0 start, 1 Q in, 2 first chunk landed, 3 chunks done, 4 the CTA states of
     // the cluster in place, 5 cluster merge done (output or parked group state), 6 CTA end; 10 second
     // chunk landed, 11 second chunk computed, 12 last chunk landed (when there are more than two);
@@ -94,7 +98,6 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
             a.trace[((static_cast<size_t>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x) * 16 + ev] =
                 globaltimer();
     };
-    stamp(0);
     // grid (splits, kv heads, work items): the CTAs of one wave cover every kv head, so their K/V
     // reads spread over whole pages of the pool
     const int w = blockIdx.z, sp = blockIdx.x, g = blockIdx.y;
@@ -139,8 +142,19 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         prefetch_tensormap(&tkv.m[g]);
         const uint64_t pol_kv = policy_evict_first();  // K/V are read once per step: keep L2 for the rest
         const int box_bytes = 2 * a.page_size * D * 2;
+        // leading chunks of positions before the span only (not on a sliding-window layer, whose
+        // ring slots the QKV projection overwrites): issued before the wait
+        int pre = 0;
+        while (a.window == 0 && pre < min(n_ch, S::NBUF) &&
+               min(g0 + (c_lo + pre + 1) * kAttnChunk, g1) <= L)
+            ++pre;
+        bool waited = false;
         for (int ch = 0; ch < n_ch; ++ch) {
             const int buf = ch % S::NBUF;
+            if (ch == pre) {
+                pdl_wait();
+                waited = true;
+            }
             if (ch >= S::NBUF && !mbar_wait(&empty[buf], ((ch / S::NBUF) - 1) & 1)) {
                 if (lane == 0) set_status(a.status, SDV_ERR_DEVICE_TIMEOUT);
                 break;
@@ -162,7 +176,10 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
                 tma_load_5d_hint(kb + (si - s_first) * box_bytes, &tkv.m[g], &full[buf], 0, 0, 0, 0,
                                  a.layer * a.n_pages + page, pol_kv);
         }
+        if (!waited) pdl_wait();
     } else {
+        pdl_wait();
+        stamp(0);
         // Q rows j = i_local * grp + hh (span row q0 + i_local, head g*grp + hh), both planes
         for (int e = tid; e < 2 * Mpad * CH; e += kGrpConsumers) {
             const int pl = e / (Mpad * CH), j = (e / CH) % Mpad, c = e % CH;

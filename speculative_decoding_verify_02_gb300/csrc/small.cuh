@@ -89,8 +89,9 @@ struct PrepArgs {
 
 // Block 0: validate the spans, record bases/offsets/row maps, advance lengths,
 // build the attention work list. Blocks 1..max_rows: embed row blockIdx.x-1.
+// It does not let its dependents start early: every later kernel of the forward starts after it
+// has finished, so what it (and any kernel before it) wrote may be read before their own wait.
 __global__ void prepare_kernel(PrepArgs p) {
-    pdl_trigger();
     pdl_wait();
     DevState &s = p.s;
     __shared__ int ok_s;
