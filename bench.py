@@ -44,7 +44,8 @@ N_LAYERS = 36
 GEMM_BYTES_PER_LAYER = 201_850_880
 GEMM_BYTES = {"qkv": 31_457_280, "o": 20_971_520, "gate_up": 99_614_720, "down": 49_807_360,
               "lm_head": 777_912_320}
-WEIGHT_BYTES_PER_STEP = 8_044_936_192      # 36 x (201,850,880 + 10,752 norm gains) + LM head + final norm
+# weights streamed per 36-layer step: 36 x (201,850,880 + 10,752 norm gains) + LM head + final norm
+# = 8,044,936,192 B
 KV_BYTES_PER_TOKEN = 147_456               # 2 (K,V) x 8 heads x 128 x 2 B x 36 layers
 EMBED_BYTES_PER_ROW = 2560 * 2
 # DRAM bytes (read + write) that ncu measured per launch of the weight-streaming GEMM, in a
@@ -514,7 +515,9 @@ def run_verify_workload(args, name, contexts, seed, dev, steps=None, warmup=None
     mean_ctx = (L0 + L0 + committed) / 2 / B
     step_ms = ms / steps
     S = K_DRAFT + 1
-    step_bytes = WEIGHT_BYTES_PER_STEP + B * (mean_ctx + S) * KV_BYTES_PER_TOKEN + B * S * EMBED_BYTES_PER_ROW
+    L = shape.n_layers
+    step_bytes = (L * (GEMM_BYTES_PER_LAYER + 10_752) + GEMM_BYTES["lm_head"] + 5120
+                  + B * (mean_ctx + S) * KV_BYTES_PER_TOKEN * L / N_LAYERS + B * S * EMBED_BYTES_PER_ROW)
     peak, peak_kind = peaks()
     return {
         "metric": f"committed tok/s (4B-shape verify, K=7, {name})",
