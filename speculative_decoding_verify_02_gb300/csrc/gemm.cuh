@@ -203,6 +203,7 @@ __device__ __forceinline__ void qkv_gains(const GemmArgs &a, const EpiLayer &el,
 __device__ __forceinline__ void epi_qkv_core(const GemmArgs &a, const EpiLayer &el, float rstd, int tile, int r,
                                              int lane, float (&x)[4], const QkvRow &q, const float (&g)[4]) {
     const int D = a.D;
+    const int dsh = D == 128 ? 7 : 6;  // head_dim is 64 or 128: head and dim of a feature by shift and mask
     int fbase;  // first feature of the tile inside its section (0 = q, 1 = k, 2 = v)
     const int section = qkv_section(a, tile, fbase);
 #pragma unroll
@@ -236,7 +237,7 @@ __device__ __forceinline__ void epi_qkv_core(const GemmArgs &a, const EpiLayer &
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int fs = fbase + lane + 32 * i;
-            const size_t o = (static_cast<size_t>(r) * a.nq + fs / D) * D + fs % D;
+            const size_t o = (static_cast<size_t>(r) * a.nq + (fs >> dsh)) * D + (fs & (D - 1));
             const Bf16Pair pr = split_bf16(x[i]);
             a.q_out[o] = pr.hi;
             a.q_out[o + static_cast<size_t>(a.rows_cap) * a.nq * D] = pr.lo;
@@ -250,6 +251,7 @@ __device__ __forceinline__ void epi_qkv_core(const GemmArgs &a, const EpiLayer &
     }
     // sliding-window layer: the slot about to be written holds position pos - window, which other
     // rows of this span may still attend and a rejection must give back; keep it first
+    const int slot = (a.page_size & (a.page_size - 1)) == 0 ? pos & (a.page_size - 1) : pos % a.page_size;
     bf16 *keep = nullptr;
     if (a.swa_backup != nullptr && q.span_row >= 0 && q.span_row < a.max_span)
         keep = a.swa_backup + ((static_cast<size_t>(a.row_seq[r]) * a.max_span + q.span_row) * 2 + (section - 1)) *
@@ -258,8 +260,8 @@ __device__ __forceinline__ void epi_qkv_core(const GemmArgs &a, const EpiLayer &
     for (int i = 0; i < 4; ++i) {
         const int fs = fbase + lane + 32 * i;
         const size_t off =
-            (((static_cast<size_t>(page) * 2 + (section - 1)) * a.nkv + fs / D) * a.page_size + pos % a.page_size) * D +
-            fs % D;
+            (((static_cast<size_t>(page) * 2 + (section - 1)) * a.nkv + (fs >> dsh)) * a.page_size + slot) * D +
+            (fs & (D - 1));
         if (keep != nullptr) keep[fs] = el.kv_layer[off];
         el.kv_layer[off] = __float2bfloat16(x[i]);
     }

@@ -7,7 +7,8 @@ each, so one attention launch merges several groups of several sequences), and
 one sequence over a 32768-token cache. The oracle runs its verify step on the
 K/V the GPU wrote during the prefill (read back through the page table), which
 keeps the oracle's cost to the verify itself; the GPU-written K/V is checked
-against an oracle prefill elsewhere (tests/test_gpu_4b.py, 848 tokens).
+against an oracle prefill here for the first 512 tokens of two of the batch-16
+sequences, and in tests/test_gpu_4b.py at 848 tokens.
 """
 import numpy as np
 import pytest
@@ -201,6 +202,42 @@ def _verify_over_gpu_kv(model, lens, S, name):
         assert tab[b, :npg[b]].tolist() == opool.table[b], b
     assert top == len(opool.free)
     print(f"{name}: max |dlogit| {worst:.3e}, {checked}/{B} sequences exact, near-tie flips {flips_all}")
+    v.close()
+
+
+def test_prefill_kv_of_two_batch16_sequences(model):
+    """The paged K/V the GPU prefill writes, every position of both layers, against the oracle's
+    prefill (its cache rounded to bf16 like the pool): the first 512 tokens of two of config 3's
+    sequences, prefilled together in 128-row chunks."""
+    import torch
+    from speculative_decoding_verify_02_gb300 import Verifier
+    from speculative_decoding_verify_02_gb300.runner import SpecLoop
+    host, dev, om = model
+    n = 512
+    prompts = [workloads.uniform_context(3, n, SHAPE.vocab, name=f"b16.ctx.{b}") for b in (0, 1)]
+    caches = [oracle.SeqCache(SHAPE, n + 8, kv_dtype="bf16") for _ in prompts]
+    for c, p in zip(caches, prompts):
+        om.forward([c], [p], last_row_logits=True)
+    v = Verifier(SHAPE, dev, page_size=P, n_pages=2 * n // P + 8, max_batch=2, max_rows=128, max_span=128,
+                 max_context=n + 64)
+    SpecLoop(v, 2, 8).prefill(prompts, chunk=128)
+    assert v.get_status() == 0
+    tab, _, _ = page_tables(v)
+    nkv, D = SHAPE.n_kv_heads, SHAPE.head_dim
+    pool = v.pool.view(torch.bfloat16).view(SHAPE.n_layers, v.ccfg.n_pages, 2, nkv, P, D)
+    same = total = 0
+    worst = 0.0
+    for b in range(2):
+        pages = torch.as_tensor(tab[b, :n // P].astype(np.int64), device="cuda")
+        for l in range(SHAPE.n_layers):
+            kv = pool[l].index_select(0, pages).permute(1, 0, 3, 2, 4).reshape(2, n, nkv, D).double().cpu().numpy()
+            for which, ref in ((0, caches[b].K[l][:n]), (1, caches[b].V[l][:n])):
+                np.testing.assert_allclose(kv[which], ref, atol=3e-2, rtol=2e-2)
+                worst = max(worst, float(np.abs(kv[which] - ref).max()))
+                same += int((kv[which] == ref).sum())
+                total += kv[which].size
+    print(f"prefill K/V of two batch-16 sequences: {same / total:.4f} of the values bit-identical, "
+          f"max |d| {worst:.3e}")
     v.close()
 
 
