@@ -76,19 +76,23 @@ __device__ __forceinline__ void gemm_stamp(const GemmArgs &a, int ev) {
 }
 
 // Shared memory given to the stage ring of one GEMM CTA. 104 KB lets two CTAs share an SM (the
-// next kernel's CTAs then start streaming weights while this one finishes).
+// next kernel's CTAs then start streaming weights while this one finishes). A launch whose grid
+// fits on the SMs one CTA each may take the deep ring instead (200 KB: twice the weight bytes in
+// flight per SM); the gate/up projection does (its 152 tiles of the 4B shape fill the SMs
+// exactly): at batch 1 it streams at 8.1 instead of 6.2 TB/s between first and last MMA.
 #ifndef SDV_GEMM_STAGE_KB
 #define SDV_GEMM_STAGE_KB 104
 #endif
+constexpr int kDeepRingKB = 200;
 
-template <int N>
+template <int N, int STAGE_KB = SDV_GEMM_STAGE_KB>
 struct GemmShape {
     static constexpr int BM = 128, BK = 64;
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_PLANE = N * BK * 2;      // one of the hi / lo planes
     static constexpr int B_BYTES = 2 * B_PLANE;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES_RAW = (SDV_GEMM_STAGE_KB * 1024) / STAGE_BYTES;
+    static constexpr int STAGES_RAW = (STAGE_KB * 1024) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 16 ? 16 : STAGES_RAW;
     // The hi and lo planes are adjacent in the B stage (N rows each), so one MMA of width 2N
     // covers both: hi product in accumulator columns [0, N), lo product in [N, 2N). One MMA per
@@ -105,7 +109,8 @@ struct GemmShape {
     static_assert(2 * TMEM_COLS <= 512, "two co-resident CTAs must fit in the SM's 512 TMEM columns");
     // the fp32 row tile [N][128] that the epilogue parks reuses the stage memory
     static_assert(N * 128 * 4 <= STAGES * STAGE_BYTES, "parked row tile must fit in the stage ring");
-    static_assert(2 * (SMEM_BYTES + 1024) <= 227 * 1024, "two CTAs per SM must fit in shared memory");
+    static_assert(STAGE_KB > 112 || 2 * (SMEM_BYTES + 1024) <= 227 * 1024, "two CTAs per SM must fit in shared memory");
+    static_assert(SMEM_BYTES + 2048 <= 227 * 1024, "one CTA must fit in shared memory");
 };
 
 constexpr int kGemmThreads = 192;
@@ -460,11 +465,11 @@ __device__ __forceinline__ void prefetch_a(const CUtensorMap *tmA0, const CUtens
 }
 
 
-template <int N, int KIND>
+template <int N, int KIND, int RING_KB = SDV_GEMM_STAGE_KB>
 __global__ void __launch_bounds__(kGemmThreads, 2)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
-    using S = GemmShape<N>;
+    using S = GemmShape<N, RING_KB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full_bar[S::STAGES], empty_bar[S::STAGES], accum_bar;

@@ -433,10 +433,12 @@ cudaError_t launch_cluster(const sdv_ctx *ctx, void (*kern)(KArgs...), dim3 grid
 template <int N, int KIND>
 cudaError_t launch_gemm_nk(const sdv_ctx *ctx, const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &a2,
                            const CUtensorMap &b, const GemmArgs &args, int grid, cudaStream_t st) {
+    // the gate/up projection takes the deep ring when its grid fits on the SMs, one CTA each
+    const bool deep = KIND == EPI_SWIGLU && grid <= ctx->sm_count;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kGemmThreads);
-    cfg.dynamicSmemBytes = GemmShape<N>::SMEM_BYTES;
+    cfg.dynamicSmemBytes = deep ? GemmShape<N, kDeepRingKB>::SMEM_BYTES : GemmShape<N>::SMEM_BYTES;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     int na = 0;
@@ -454,6 +456,8 @@ cudaError_t launch_gemm_nk(const sdv_ctx *ctx, const CUtensorMap &a0, const CUte
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
+    if constexpr (KIND == EPI_SWIGLU)
+        if (deep) return cudaLaunchKernelEx(&cfg, gemm_kernel<N, KIND, kDeepRingKB>, a0, a1, a2, b, args);
     return cudaLaunchKernelEx(&cfg, gemm_kernel<N, KIND>, a0, a1, a2, b, args);
 }
 
@@ -495,6 +499,7 @@ cudaError_t set_gemm_smem() {
     if (e == cudaSuccess) e = set_smem(gemm_kernel<N, EPI_RESID>, GemmShape<N>::SMEM_BYTES);
     if (e == cudaSuccess) e = set_smem(gemm_kernel<N, EPI_SWIGLU>, GemmShape<N>::SMEM_BYTES);
     if (e == cudaSuccess) e = set_smem(gemm_kernel<N, EPI_LMHEAD>, GemmShape<N>::SMEM_BYTES);
+    if (e == cudaSuccess) e = set_smem(gemm_kernel<N, EPI_SWIGLU, kDeepRingKB>, GemmShape<N, kDeepRingKB>::SMEM_BYTES);
     return e;
 }
 
