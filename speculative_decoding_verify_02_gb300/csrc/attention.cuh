@@ -40,6 +40,7 @@ struct AttnArgs {
     size_t out_plane;        // 0: write the hi plane only (a plain bf16 output)
     int *status;
     int splits;              // attention_group.cuh: CTAs sharing one group's chunks (1, 2, 4 or 8)
+    int group;               // attention_group.cuh: key positions per group (1024 or 2048)
     int p_lo;                // attention_group.cuh: 1 = probabilities as a hi/lo pair, 0 = bf16 only
     int layer;               // attention_group.cuh: layer index in the pool tensor map
     int merge_groups;        // attention_group.cuh: sequences of up to this many key groups are merged

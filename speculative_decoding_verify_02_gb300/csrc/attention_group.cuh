@@ -2,9 +2,10 @@
 // [layer*page][K|V][kv head][slot][dim], and one 128-key chunk of a kv head is, per page, a box of
 // (page size) rows x 64 dims per half of the head dimension, landing 128-byte swizzled.
 //
-// A (sequence, 1024-position key group, kv head) is served by one thread-block cluster of
-// `splits` CTAs, each owning 8 / splits consecutive 128-key chunks of the group (the split is fixed
-// per configuration, so a row's arithmetic never depends on the span or the batch). In each CTA one
+// A (sequence, key group, kv head) is served by one thread-block cluster of `splits` CTAs, each
+// owning group / 128 / splits consecutive 128-key chunks of the group; the group (1024 positions,
+// or 2048 where that brings a long sequence's grid into one wave) and the split are fixed per
+// configuration, so a row's arithmetic never depends on the span or the batch. In each CTA one
 // producer warp issues the chunks' K/V copies into a ring of three buffers, refilling a buffer as
 // soon as every consumer warp released it, and eight consumer warps walk the chunks in position
 // order keeping an online softmax (running max m, sum l, unnormalised o) per query row. At most 32
@@ -34,11 +35,11 @@ constexpr int kMaxKvHeads = 16;
 struct KvMaps {
     CUtensorMap m[kMaxKvHeads];
 };
-constexpr int kGrpChunks = kAttnGroup / kAttnChunk;  // 8 chunks of 128 keys
+constexpr int kGrpMaxSplits = kAttnCluster;         // CTAs of a group's cluster: 1, 2, 4 or 8
 constexpr int kGrpRows = 32;                         // query rows (heads x span rows) per launch
 constexpr int kGrpQuarters = 4;                      // fixed key partition of a chunk
 constexpr int kGrpQKeys = kAttnChunk / kGrpQuarters;
-// sequences of up to this many 1024-position key groups are merged across groups inside the
+// sequences of up to this many key groups are merged across groups inside the
 // attention kernel (by the last group CTA to finish); longer ones by attn_merge_kernel
 constexpr int kInKernelMergeGroups = 8;
 
@@ -110,10 +111,10 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     if (ni == 0) return;
     const int M = a.grp * ni, Mpad = (M + 15) & ~15;
     const int key_end = L + S_b;
-    const int n_groups = (key_end + kAttnGroup - 1) / kAttnGroup;
-    const int g0 = grp_idx * kAttnGroup, g1 = min(g0 + kAttnGroup, key_end);
+    const int n_groups = (key_end + a.group - 1) / a.group;
+    const int g0 = grp_idx * a.group, g1 = min(g0 + a.group, key_end);
     const int n_ch_group = (g1 - g0 + kAttnChunk - 1) / kAttnChunk;
-    const int c_per = kGrpChunks / a.splits;
+    const int c_per = a.group / kAttnChunk / a.splits;
     // this CTA's chunks (may be none); on a sliding-window layer the chunks below every span row's
     // window are skipped (all their keys are masked, so they would leave the state unchanged)
     const int win_lo = a.window > 0 ? max(0, L - a.window + 1) : 0;
@@ -428,11 +429,11 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     const uint32_t cs_l = smem_u32(cs);
     for (int it = tid; it < (j1 - j0) * (D / 4); it += kGrpThreads) {
         const int j = j0 + it / (D / 4), d = (it % (D / 4)) * 4;
-        float2 ml[kGrpChunks];
-        float4 x[kGrpChunks];
+        float2 ml[kGrpMaxSplits];
+        float4 x[kGrpMaxSplits];
         float Mx = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < kGrpChunks; ++c) {
+        for (int c = 0; c < kGrpMaxSplits; ++c) {
             if (c < a.splits) {
                 const uint32_t row = mapa_shared(cs_l, static_cast<uint32_t>(c)) + j * S::QO_LD * 4;
                 ml[c] = ld_dsmem_f2(row + D * 4);
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         float den = 0.f;
         float4 n = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < kGrpChunks; ++c) {
+        for (int c = 0; c < kGrpMaxSplits; ++c) {
             if (c < a.splits) {
                 const float wq = ml[c].x == -INFINITY ? 0.f : exp2f(ml[c].x - Mx);
                 den += wq * ml[c].y;

@@ -81,6 +81,7 @@ struct sdv_ctx {
     float2 *attn_pml = nullptr;
     int *attn_cnt = nullptr;
     int attn_splits = 1;
+    int attn_group = kAttnGroup;  // key positions per attention group (1024, or 2048 for long sequences)
     int attn_lo = 1;  // attention products with hi/lo pairs (queries and probabilities)
     unsigned long long *trace = nullptr;  // caller's timeline buffer (sdv_fwd_trace), or nullptr
     size_t trace_words = 0;
@@ -185,7 +186,25 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     const int pps = ceil_div(c.max_context, c.page_size);
     const int grp = m.n_q_heads / m.n_kv_heads;
     const int qrows = kAttnRows / grp;
-    const int work_cap = ceil_div(static_cast<long long>(c.n_pages) * c.page_size, kAttnGroup) + B;
+    // attention: CTAs (one cluster) per (key group, kv head), fixed by the configuration (a row's
+    // arithmetic must not depend on the span): the largest power of two <= 8 that keeps the grid
+    // within four CTAs per SM for a full batch at full context and groups x splits <= 64. Groups
+    // hold 1024 positions; where that leaves one CTA per group and doubling the group brings a
+    // full-size grid into one wave of CTAs (long single sequences), 2048 (the TMA-fed kernel only).
+    int group = kAttnGroup;
+    int max_groups = ceil_div(c.max_context, group);
+    int splits = 8;
+    while (splits > 1 && (static_cast<long long>(B) * max_groups * m.n_kv_heads * splits > 4LL * sm_count ||
+                          max_groups * splits > 64))
+        splits >>= 1;
+    const bool tma_attn = c.page_size >= 8 && c.page_size <= kAttnChunk && (c.page_size & (c.page_size - 1)) == 0 &&
+                          m.n_kv_heads <= kMaxKvHeads;
+    if (tma_attn && splits == 1 &&
+        static_cast<long long>(B) * ceil_div(c.max_context, 2 * kAttnGroup) * m.n_kv_heads <= sm_count) {
+        group = 2 * kAttnGroup;
+        max_groups = ceil_div(c.max_context, group);
+    }
+    const int work_cap = ceil_div(static_cast<long long>(c.n_pages) * c.page_size, group) + B;
     const int ng_slots = c.ngram_capacity > 0 ? next_pow2(std::max(16, 2 * c.ngram_capacity)) : 0;
     const int ng_orders = ngram_orders(c);
     const int ss_tiles = ceil_div(H, 128);
@@ -252,14 +271,6 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     int *done_lm = reinterpret_cast<int *>(take(sizeof(int)));
     auto *keys = reinterpret_cast<unsigned long long *>(take(sizeof(unsigned long long) * kRowsCap));
     float2 *rope = reinterpret_cast<float2 *>(take(sizeof(float2) * static_cast<size_t>(c.max_context) * (D / 2)));
-    // attention: CTAs (one cluster) per (group, kv head), fixed by the configuration (a row's
-    // arithmetic must not depend on the span): the largest power of two <= 8 that keeps the grid
-    // within four CTAs per SM for a full batch at full context and groups x splits <= 64
-    const int max_groups = ceil_div(c.max_context, kAttnGroup);
-    int splits = 8;
-    while (splits > 1 && (static_cast<long long>(B) * max_groups * m.n_kv_heads * splits > 4LL * sm_count ||
-                          max_groups * splits > 64))
-        splits >>= 1;
     const size_t nslots = static_cast<size_t>(work_cap) * splits * m.n_kv_heads * grp * qrows;
     float *apo = reinterpret_cast<float *>(take(sizeof(float) * nslots * D));
     float2 *apml = reinterpret_cast<float2 *>(take(sizeof(float2) * nslots));
@@ -288,6 +299,7 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
         ctx->attn_pml = apml;
         ctx->attn_cnt = acnt;
         ctx->attn_splits = splits;
+        ctx->attn_group = group;
         ctx->ss_tiles = ss_tiles;
         ctx->grp = grp;
         ctx->qrows = qrows;
@@ -567,6 +579,7 @@ int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *
     a.out = out;
     a.status = ctx->st.status;
     a.splits = ctx->attn_splits;
+    a.group = ctx->attn_group;
     a.layer = layer;
     if ((ctx->swa_mask >> layer) & 1ull) {
         a.window = m.swa_window;
@@ -601,7 +614,7 @@ int run_attention(sdv_ctx *ctx, int layer, const bf16 *q, size_t q_plane, bf16 *
     // CTAs to share the rows (up to kInKernelMergeGroups groups), else by attn_merge_kernel, which
     // is launched only when the configuration allows such sequences.
     a.merge_groups = ctx->attn_splits >= 4 ? kInKernelMergeGroups : 1;
-    const bool merge = ceil_div(static_cast<long long>(ctx->c.max_context), kAttnGroup) > a.merge_groups;
+    const bool merge = ceil_div(static_cast<long long>(ctx->c.max_context), ctx->attn_group) > a.merge_groups;
     const dim3 mgrid(ceil_div(kGrpRows, kMergeRows), m.n_kv_heads, B);
     for (int q0 = 0; q0 < max_span; q0 += a.qrows) {
         a.q0 = q0;
@@ -634,7 +647,7 @@ int prepare(sdv_ctx *ctx, const int32_t *tokens, const int32_t *row_off, const i
     p.B = B;
     p.max_rows = max_rows;
     p.max_span = max_span;
-    p.chunk = kAttnGroup;
+    p.chunk = ctx->attn_group;
     p.embed = embed;
     p.E = static_cast<const bf16 *>(ctx->w.embed);
     p.g0 = static_cast<const bf16 *>(ctx->layers[0].attn_norm);
