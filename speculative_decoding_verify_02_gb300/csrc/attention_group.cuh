@@ -376,6 +376,58 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
         }
     }
     __syncthreads();
+    auto store = [&](int j, int d, float v) {
+        const int r = row0 + a.q0 + j / a.grp, h = g * a.grp + j % a.grp;
+        const size_t oi = (static_cast<size_t>(r) * a.nq + h) * D + d;
+        const Bf16Pair pr = split_bf16(v);
+        a.out[oi] = pr.hi;
+        if (a.out_plane) a.out[oi + a.out_plane] = pr.lo;
+    };
+    const bool multi = n_groups > 1;
+    const size_t rowsw = static_cast<size_t>(a.grp) * a.qrows;
+    const size_t gslot = static_cast<size_t>(w) * a.nkv + g;  // this group's parked state (multi)
+    if (a.splits == 1) {
+        // One CTA per group: merging its quarters gives the group's state directly, the output of
+        // a single-group sequence or the state parked for the merge across groups (the same values
+        // the cluster merge below gives with one split, whose weight is exactly 1).
+        for (int e = tid; e < M * (D / 4); e += kGrpThreads) {
+            const int j = e / (D / 4), d = (e % (D / 4)) * 4;
+            float2 st[kGrpQuarters];
+            float Mx = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kGrpQuarters; ++k) {
+                st[k] = *reinterpret_cast<const float2 *>(&qo[(k * kGrpRows + j) * S::QO_LD + D]);
+                Mx = fmaxf(Mx, st[k].x);
+            }
+            float wq[kGrpQuarters];
+#pragma unroll
+            for (int k = 0; k < kGrpQuarters; ++k) wq[k] = st[k].x == -INFINITY ? 0.f : exp2f(st[k].x - Mx);
+            float l = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < kGrpQuarters; ++k) {
+                l += wq[k] * st[k].y;
+                const float4 x = *reinterpret_cast<const float4 *>(&qo[(k * kGrpRows + j) * S::QO_LD + d]);
+                acc.x += wq[k] * x.x;
+                acc.y += wq[k] * x.y;
+                acc.z += wq[k] * x.z;
+                acc.w += wq[k] * x.w;
+            }
+            if (!multi) {
+                store(j, d, acc.x / l);
+                store(j, d + 1, acc.y / l);
+                store(j, d + 2, acc.z / l);
+                store(j, d + 3, acc.w / l);
+            } else {
+                *reinterpret_cast<float4 *>(&a.part_o[(gslot * rowsw + j) * D + d]) = acc;
+                if (d == 0) a.part_ml[gslot * rowsw + j] = make_float2(Mx, l);
+            }
+        }
+        stamp(4);
+        stamp(5);
+        stamp(6);
+        return;  // sequences of several groups are merged by attn_merge_kernel
+    }
     // the CTA's state: quarters merged per row in quarter order -> cs [row][QO_LD] (o, then m, l)
     float *cs = qo + S::RECV_OFF / 4;
     for (int e = tid; e < M * (D / 4 + 1); e += kGrpThreads) {
@@ -411,21 +463,11 @@ __global__ void __launch_bounds__(kGrpThreads, 1)
     cluster_sync();  // every CTA's state of the group in place
     stamp(4);
 
-    auto store = [&](int j, int d, float v) {
-        const int r = row0 + a.q0 + j / a.grp, h = g * a.grp + j % a.grp;
-        const size_t oi = (static_cast<size_t>(r) * a.nq + h) * D + d;
-        const Bf16Pair pr = split_bf16(v);
-        a.out[oi] = pr.hi;
-        if (a.out_plane) a.out[oi + a.out_plane] = pr.lo;
-    };
     // Cluster merge: CTA `sp` finishes rows [j0, j1) over the splits' states, in split (position)
     // order, reading the other CTAs' shared memory. With one key group that is the output;
     // otherwise the group's (o, m, l) is parked for the merge across groups.
     const int per = (M + a.splits - 1) / a.splits;
     const int j0 = min(M, sp * per), j1 = min(M, j0 + per);
-    const bool multi = n_groups > 1;
-    const size_t rowsw = static_cast<size_t>(a.grp) * a.qrows;
-    const size_t gslot = static_cast<size_t>(w) * a.nkv + g;  // this group's parked state (multi)
     const uint32_t cs_l = smem_u32(cs);
     for (int it = tid; it < (j1 - j0) * (D / 4); it += kGrpThreads) {
         const int j = j0 + it / (D / 4), d = (it % (D / 4)) * 4;
