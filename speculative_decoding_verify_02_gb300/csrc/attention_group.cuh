@@ -619,11 +619,17 @@ __global__ void __launch_bounds__(kMergeRows * D / 4)
     if (j >= M) return;
     const size_t rowsw = static_cast<size_t>(a.grp) * a.qrows;
     auto slot = [&](int q) { return ((static_cast<size_t>(w0) + q) * a.nkv + g) * rowsw + j; };
+    constexpr int QB = 8;  // groups whose loads are in flight together
     float Mx = -INFINITY;
-    for (int q = 0; q < n_groups; ++q) Mx = fmaxf(Mx, __ldcg(&a.part_ml[slot(q)]).x);
+    for (int q0 = 0; q0 < n_groups; q0 += QB) {
+        float mx[QB];
+#pragma unroll
+        for (int k = 0; k < QB; ++k) mx[k] = q0 + k < n_groups ? __ldcg(&a.part_ml[slot(q0 + k)]).x : -INFINITY;
+#pragma unroll
+        for (int k = 0; k < QB; ++k) Mx = fmaxf(Mx, mx[k]);
+    }
     float den = 0.f;
     float4 n = make_float4(0.f, 0.f, 0.f, 0.f);
-    constexpr int QB = 8;  // groups whose loads are in flight together
     for (int q0 = 0; q0 < n_groups; q0 += QB) {
         float2 ml[QB];
         float4 x[QB];
