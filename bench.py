@@ -51,7 +51,7 @@ EMBED_BYTES_PER_ROW = 2560 * 2
 # DRAM bytes (read + write) that ncu measured per launch of the weight-streaming GEMM, in a
 # 2-layer case of the same shapes (profiles/gemm_tcgen05_qwen3_4b_verify_N16.md); a launch streams
 # its own weights, so a 36-layer step is 36 layers of the first four plus one LM head.
-GEMM_TRAFFIC_MB = {"qkv": 31.7002, "o": 21.3691, "gate_up": 99.9084, "down": 50.5654, "lm_head": 778.3137}
+GEMM_TRAFFIC_MB = {"qkv": 31.6983, "o": 21.3682, "gate_up": 99.9138, "down": 50.5648, "lm_head": 778.4595}
 from speculative_decoding_verify_02_gb300 import TRACE_REGION_CTAS, TRACE_STAMPS  # noqa: E402
 TRACE_REGION_WORDS = TRACE_REGION_CTAS * TRACE_STAMPS  # sdv_fwd_trace: one region per launch
 PROJ = ("qkv", "o", "gate_up", "down")

@@ -27,6 +27,7 @@ struct GemmArgs {
     int kind;
     int tiles, splits, kps, k_blocks;  // output tiles, K splits, k-blocks per split, total k-blocks (64 wide)
     int l2_ahead;                      // k-blocks prefetched into L2 beyond the shared-memory stages
+    int deep_ring;                     // host: launched with the deep stage ring
     int n_out;                         // valid output features (ffn for SwiGLU)
     int rows_cap;                      // rows of the activation / ss buffers (plane stride in rows)
     const int *nrows;                  // device: rows present (R)
@@ -78,8 +79,10 @@ __device__ __forceinline__ void gemm_stamp(const GemmArgs &a, int ev) {
 // Shared memory given to the stage ring of one GEMM CTA. 104 KB lets two CTAs share an SM (the
 // next kernel's CTAs then start streaming weights while this one finishes). A launch whose grid
 // fits on the SMs one CTA each may take the deep ring instead (200 KB: twice the weight bytes in
-// flight per SM); the gate/up projection does (its 152 tiles of the 4B shape fill the SMs
-// exactly): at batch 1 it streams at 8.1 instead of 6.2 TB/s between first and last MMA.
+// flight per SM; four stages instead of two at N = 128). The gate/up projection does (its 152
+// tiles of the 4B shape fill the SMs exactly): at batch 1 it streams at 8.1 instead of 6.2 TB/s
+// between first and last MMA. So does the down projection, with the split count at which all its
+// clusters of 200 KB CTAs are resident at once.
 #ifndef SDV_GEMM_STAGE_KB
 #define SDV_GEMM_STAGE_KB 104
 #endif
