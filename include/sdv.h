@@ -111,7 +111,9 @@ typedef struct {
 
 /* Bytes of the caller-owned workspace (scratch, the device status word, page
  * tables, lengths, the n-gram index and loop state). Allocate with 256-byte
- * alignment; the library zero-initialises what it needs in sdv_create. */
+ * alignment; the library zero-initialises what it needs in sdv_create. The
+ * size depends on the configuration and on the current device's SM count (the
+ * attention's work layout), so ask on the device the context will use. */
 int sdv_workspace_bytes(const sdv_model_cfg *m, const sdv_cache_cfg *c, size_t *bytes);
 
 /* Bytes of the caller-owned KV pool. Layout (bf16):

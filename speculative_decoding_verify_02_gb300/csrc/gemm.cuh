@@ -36,10 +36,6 @@ struct GemmArgs {
     const float *ss_in;
     int ss_tiles, hidden;
     float eps;
-    // split-K
-    float *partial;
-    int *counters;
-    int part_stride;                   // features per partial row (tiles * 128)
     // QKV epilogue
     int nq, nkv, D, q_tiles, k_tiles, qk_norm;
     const bf16 *q_gain, *k_gain;

@@ -111,8 +111,6 @@ struct sdv_ctx {
     DevState st{};
     float *x = nullptr, *ss = nullptr;
     bf16 *xb = nullptr, *q = nullptr, *attn_o = nullptr, *h = nullptr;
-    float *part[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
-    int *cnt[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
     int *done_lm = nullptr;
     unsigned long long *keys = nullptr;
     float2 *rope = nullptr;
@@ -297,13 +295,6 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
     bf16 *q = reinterpret_cast<bf16 *>(take(sizeof(bf16) * 2 * kRowsCap * qdim));
     bf16 *ao = reinterpret_cast<bf16 *>(take(sizeof(bf16) * 2 * kRowsCap * qdim));
     bf16 *hb = reinterpret_cast<bf16 *>(take(sizeof(bf16) * 2 * kRowsCap * F));
-    float *part[5];
-    int *cnt[5];
-    for (int i = 0; i < 5; ++i) {
-        const size_t n = plans[i].splits > 1 ? static_cast<size_t>(plans[i].splits) * kRowsCap * plans[i].tiles * 128 : 0;
-        part[i] = reinterpret_cast<float *>(take(sizeof(float) * n));
-        cnt[i] = reinterpret_cast<int *>(take(sizeof(int) * plans[i].tiles));
-    }
     // sliding-window backups: per local layer [max_batch][max_span][K|V][nkv][D]
     const int n_local = __builtin_popcountll(local_mask(m));
     const size_t swa_layer = static_cast<size_t>(B) * c.max_span * 2 * kvdim;
@@ -324,11 +315,7 @@ size_t carve(const sdv_model_cfg &m, const sdv_cache_cfg &c, sdv_ctx *ctx, uint8
         ctx->q = q;
         ctx->attn_o = ao;
         ctx->h = hb;
-        for (int i = 0; i < 5; ++i) {
-            ctx->part[i] = part[i];
-            ctx->cnt[i] = cnt[i];
-            ctx->plan[i] = plans[i];
-        }
+        for (int i = 0; i < 5; ++i) ctx->plan[i] = plans[i];
         ctx->done_lm = done_lm;
         ctx->swa_backup = swa_backup;
         ctx->swa_layer_elems = swa_layer;
@@ -580,9 +567,6 @@ GemmArgs base_args(const sdv_ctx *ctx, int kind, int pidx, int layer) {
     a.ss_tiles = ctx->ss_tiles;
     a.hidden = ctx->m.hidden;
     a.eps = ctx->m.rms_eps;
-    a.partial = ctx->part[pidx];
-    a.counters = ctx->cnt[pidx];
-    a.part_stride = p.tiles * 128;
     a.trace = trace_region(ctx, pidx == P_LM ? 5 * ctx->m.n_layers : 5 * layer + 1 + pidx,
                            static_cast<size_t>(p.tiles) * p.splits);
     return a;
